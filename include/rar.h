@@ -1,0 +1,168 @@
+/*
+ * rar.h -- ring all-reduce over p virtual ranks held in one GPU's memory.
+ *
+ * The operation ("Ring All-Reduce, in depth", section "The schedule"):
+ * p ranks, each with an n-element buffer cut into p chunks by chunk_bounds
+ * (section "An implementation": the first n mod p chunks are one element
+ * longer).  Reduce-scatter runs p - 1 steps; at step s rank r sends chunk
+ * (r - s) mod p to rank r + 1, which combines it into its own copy, so that
+ * afterwards rank r holds the complete reduction of chunk (r + 1) mod p.
+ * All-gather runs p - 1 more steps; at step s rank r sends chunk
+ * (r + 1 - s) mod p and the receiver overwrites its copy.  Every rank ends
+ * with the elementwise reduction ("AllReduce 与 Ring 通信算法详解", section
+ * "AllReduce 语义": sum, average or maximum).
+ *
+ * Arithmetic follows the ring's hop order exactly: element i of chunk c
+ * becomes x_c[i] (+) x_(c+1)[i] (+) ... (+) x_(c+p-1)[i] (indices mod p),
+ * each (+) rounded to the buffer's dtype ("Derive the cost of a ring
+ * all-reduce", last probe: the reduction runs in the buffer's dtype), so the
+ * result is bit-identical to the schedule run on real ranks.  avg is that
+ * sum times 1/p (rounded to binary32), applied once by the chunk's owner and
+ * rounded once to binary32, then to a 16-bit dtype.  max keeps the running
+ * value unless the receiver's element is strictly greater.
+ *
+ * All p rank buffers live in the GPU's HBM; the library moves no data
+ * between GPUs.  Engines (rar_options.engine):
+ *   RAR_ENGINE_FUSED       one kernel reads every rank's element once, folds
+ *                          in hop order and stores the result to every rank
+ *                          (2 p n element moves);
+ *   RAR_ENGINE_RING        persistent executor: CTA groups play the ranks and
+ *                          run the schedule step by step, slice-pipelined,
+ *                          handing slices to the right neighbour through
+ *                          acquire/release flags (5 (p - 1) n element moves);
+ *   RAR_ENGINE_RING_BIDIR  as RING, with the buffer's second half run by a
+ *                          ring in the opposite direction ("Bidirectional
+ *                          rings" in "Ring All-Reduce, in depth", section
+ *                          "What real libraries add");
+ *   RAR_ENGINE_FUSED_TREE  one kernel, tree order over the rank index (adjacent
+ *                          pairs level by level); not bit-identical to the
+ *                          ring, float sums within 4 p 2^-24 sum|x| of exact.
+ *
+ * Conventions for every call:
+ *   - Return value: RAR_OK or a rar_status_code; rar_last_error(h) gives a
+ *     message.  Argument errors are reported synchronously and launch
+ *     nothing.  Device-side errors (a ring wait that timed out) surface
+ *     through rar_status().
+ *   - Buffers: `bufs` is a host array of p device pointers, each to n
+ *     contiguous elements on the handle's device, pairwise non-overlapping.
+ *     The caller owns them; the operation is in place.  The array itself is
+ *     read during the call only.  All pointers 16-byte aligned select the
+ *     128-bit path; otherwise a per-element path runs (same results).
+ *   - Streams: work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and the call returns without waiting.  One call
+ *     in flight per handle: calls on one stream are ordered; calls on several
+ *     streams with one handle must be ordered by the caller.
+ *   - Trivial calls: p == 1 or n == 0 return RAR_OK and launch nothing (the
+ *     torch ring in "An implementation" returns its tensor when p == 1).
+ */
+#ifndef RAR_H
+#define RAR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RAR_VERSION 1
+#define RAR_MAX_P 1024
+
+typedef struct rar_ctx *rar_handle;
+
+typedef enum { RAR_INT32 = 0, RAR_FLOAT32 = 1, RAR_BFLOAT16 = 2, RAR_FLOAT16 = 3 } rar_dtype;
+typedef enum { RAR_SUM = 0, RAR_MAX = 1, RAR_AVG = 2 } rar_op;
+typedef enum {
+    RAR_ENGINE_FUSED = 0,
+    RAR_ENGINE_RING = 1,
+    RAR_ENGINE_RING_BIDIR = 2,
+    RAR_ENGINE_FUSED_TREE = 3
+} rar_engine;
+
+typedef enum {
+    RAR_OK = 0,
+    RAR_EINVAL = 1,        /* bad argument (null, p out of range, overlap, wrong device) */
+    RAR_EUNSUPPORTED = 2,  /* valid but not offered (avg on int32, grid not co-resident) */
+    RAR_ENOMEM = 3,        /* scratch allocation failed in rar_init */
+    RAR_ECUDA = 4,         /* a CUDA runtime call failed; message in rar_last_error */
+    RAR_ETIMEOUT = 5,      /* a ring wait ran past timeout_ns (from rar_status) */
+    RAR_EABORTED = 6       /* the call was abandoned after another CTA timed out */
+} rar_status_code;
+
+typedef enum { RAR_FAULT_NONE = 0, RAR_FAULT_MUTE = 1, RAR_FAULT_DELAY = 2 } rar_fault_mode;
+
+/* Options; an all-zero struct means "defaults". */
+typedef struct {
+    int engine;                    /* rar_engine */
+    int channels;                  /* ring engines: CTAs per rank, 0 = chosen from the SM count */
+    int slice_elems;               /* ring engines: elements per pipelined slice, 0 = auto */
+    int block_threads;             /* threads per CTA (multiple of 32, <= 1024), 0 = auto */
+    unsigned long long timeout_ns; /* ring engines: bound on every wait, 0 = 2 s */
+    int skip_pointer_check;        /* nonzero: skip the per-call device-pointer query */
+    int fault_mode;                /* rar_fault_mode, ring engines only (tests) */
+    int fault_rank;                /* rank the fault applies to */
+    unsigned fault_delay_ns;       /* RAR_FAULT_DELAY: pause before each slice */
+} rar_options;
+
+/* Create a handle on `device`; allocates the ring engines' flags, counters
+ * and status word there (a few hundred KB).  opt may be NULL.
+ * Errors: RAR_EINVAL (out NULL, bad device or option), RAR_ENOMEM,
+ * RAR_ECUDA. */
+int rar_init(rar_handle *out, int device, const rar_options *opt);
+
+/* Replace the handle's options between calls (same validation as rar_init). */
+int rar_set_options(rar_handle h, const rar_options *opt);
+
+/* In-place all-reduce of p rank buffers of n elements (the whole schedule:
+ * reduce-scatter then all-gather).
+ * Errors: RAR_EINVAL (null handle/array/pointer, p < 1 or p > RAR_MAX_P,
+ * unknown dtype or op, n * element size overflows, overlapping buffers,
+ * pointers not device memory of the handle's device), RAR_EUNSUPPORTED
+ * (avg on int32; ring engine grid cannot be co-resident), RAR_ECUDA. */
+int rar_allreduce(rar_handle h, void *const *bufs, int p, size_t n, int dtype, int op,
+                  void *stream);
+
+/* The reduce-scatter half alone ("Ring All-Reduce, in depth", section
+ * "Trade-offs": the two halves are also used separately).  Afterwards rank r
+ * holds the complete reduction of chunk (r + 1) mod p in that chunk's place
+ * in its buffer (avg already scaled); its other chunks hold partial values
+ * (fused engines: unchanged inputs; ring engines: the schedule's partials).
+ * RAR_ENGINE_RING_BIDIR: the first half's chunk (r + 1) and the second
+ * half's chunk (r - 1), both by chunk_bounds of that half.
+ * Same arguments and errors as rar_allreduce. */
+int rar_reduce_scatter(rar_handle h, void *const *bufs, int p, size_t n, int dtype, int op,
+                       void *stream);
+
+/* The all-gather half alone: rank r's chunk (r + 1) mod p is copied to every
+ * other rank (RAR_ENGINE_RING_BIDIR: by the same split as in
+ * rar_reduce_scatter).  After rar_reduce_scatter this completes the
+ * all-reduce.  No arithmetic; dtype only sets the element size.
+ * Same arguments and errors as rar_allreduce (op is not taken). */
+int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, void *stream);
+
+/* Synchronise the stream of the last call and return its device-side
+ * status: RAR_OK, RAR_ETIMEOUT (a wait ran out; rar_last_error names the
+ * rank and step), or RAR_EABORTED.  A timed-out call leaves the buffers
+ * partly updated; the handle stays usable. */
+int rar_status(rar_handle h);
+
+/* Per-rank count of elements each rank sent in the last ring-engine call
+ * (the fused engines send nothing; counts are 0).  out has p entries; p must
+ * equal the last call's p.  Synchronises like rar_status.  For the full
+ * all-reduce, sends_r = 2 n - |C_(r+1)| - |C_(r+2)| ("Ring All-Reduce, in
+ * depth", "The schedule": 2 (p - 1)/p x n when p divides n). */
+int rar_send_counts(rar_handle h, unsigned long long *out, int p);
+
+/* Message for the handle's last error (never NULL; "" when none).  Valid
+ * until the next call on the handle.  h may be NULL for rar_init errors. */
+const char *rar_last_error(rar_handle h);
+
+/* Synchronise the device, free the scratch and the handle.  NULL is a no-op. */
+int rar_destroy(rar_handle h);
+
+/* RAR_VERSION of the loaded library. */
+int rar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

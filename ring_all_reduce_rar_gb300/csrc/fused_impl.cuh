@@ -1,0 +1,352 @@
+// fused_impl.cuh -- engine (a): the fused order-faithful reducer.
+//
+// The ring's data movement collapses to: every output element of chunk c is
+// x_c (+) x_(c+1) (+) ... (+) x_(c+p-1) (indices mod p) in that exact order
+// ("Ring All-Reduce, in depth", "The schedule" / "Tracing four GPUs": chunk c
+// starts at rank c and collects one contribution per hop), scaled by 1/p at
+// the owner for avg, and then copied to every rank by the all-gather.  One
+// kernel therefore reads each rank's element once and stores the result once
+// per rank: 2 p n element moves, the minimum for an in-place all-reduce.
+//
+// Work is split into tiles of blockDim.x * U 16-byte vectors, walked by a
+// grid-stride loop over a grid sized to the co-resident CTA count.  A tile
+// inside a single chunk takes the uniform path (one fold order for the whole
+// CTA, all p loads issued before the fold); tiles that cross a chunk
+// boundary or the ragged tail fall back to per-vector and per-element folds,
+// so that no vector lane ever mixes two chunks' orders.
+#pragma once
+
+#include "elem_ops.cuh"
+
+namespace rar {
+
+constexpr int kFusedThreads = 256;
+
+// Fold order for chunk c over ranks c, c+1, ..., c+p-1 on U vectors at
+// v0, v0 + stride, ..., then store per phase.
+template <int DT, int OP, int P, int U>
+__device__ __forceinline__ void fused_fold_vectors(const FusedArgs &a, int p, int c, long long v0,
+                                                   long long stride) {
+    uint4 acc[U];
+    const int phase = a.phase;
+    const int owner = (c == 0) ? p - 1 : c - 1;
+    if (phase == PHASE_AG) {
+        // all-gather alone: the owner's finished chunk goes to everyone
+        const uint4 *src = reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, p, owner));
+#pragma unroll
+        for (int u = 0; u < U; u++) acc[u] = __ldcs(src + v0 + u * stride);
+        for (int r = 0; r < p; r++) {
+            if (r == owner) continue;
+            uint4 *dst = reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, r));
+#pragma unroll
+            for (int u = 0; u < U; u++) __stcs(dst + v0 + u * stride, acc[u]);
+        }
+        return;
+    }
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, p, c));
+#pragma unroll
+        for (int u = 0; u < U; u++) acc[u] = __ldcs(src + v0 + u * stride);
+    }
+    if constexpr (P > 0) {
+        uint4 own[P > 1 ? P - 1 : 1][U];
+#pragma unroll
+        for (int k = 1; k < P; k++) {
+            int r = c + k;
+            r -= (r >= P) ? P : 0;
+            const uint4 *src = reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, P, r));
+#pragma unroll
+            for (int u = 0; u < U; u++) own[k - 1][u] = __ldcs(src + v0 + u * stride);
+        }
+#pragma unroll
+        for (int k = 1; k < P; k++)
+#pragma unroll
+            for (int u = 0; u < U; u++) acc[u] = hop_vec<DT, OP>(acc[u], own[k - 1][u]);
+    } else {
+        constexpr int G = 8;
+        for (int k0 = 1; k0 < p; k0 += G) {
+            uint4 own[G][U];
+#pragma unroll
+            for (int j = 0; j < G; j++) {
+                int k = k0 + j;
+                if (k < p) {
+                    int r = c + k;
+                    r -= (r >= p) ? p : 0;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, p, r));
+#pragma unroll
+                    for (int u = 0; u < U; u++) own[j][u] = __ldcs(src + v0 + u * stride);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < G; j++)
+                if (k0 + j < p)
+#pragma unroll
+                    for (int u = 0; u < U; u++) acc[u] = hop_vec<DT, OP>(acc[u], own[j][u]);
+        }
+    }
+    if constexpr (OP == OP_AVG) {
+#pragma unroll
+        for (int u = 0; u < U; u++) acc[u] = scale_vec<DT>(acc[u], a.inv_p);
+    }
+    if (phase == PHASE_RS) {
+        uint4 *dst = reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, owner));
+#pragma unroll
+        for (int u = 0; u < U; u++) __stcs(dst + v0 + u * stride, acc[u]);
+        return;
+    }
+    for (int r = 0; r < p; r++) {
+        uint4 *dst = reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, r));
+#pragma unroll
+        for (int u = 0; u < U; u++) __stcs(dst + v0 + u * stride, acc[u]);
+    }
+}
+
+// One element i of chunk c, same order and phases.
+template <int DT, int OP>
+__device__ __forceinline__ void fused_fold_element(const FusedArgs &a, int p, int c, long long i) {
+    const int owner = (c == 0) ? p - 1 : c - 1;
+    uint32_t acc;
+    if (a.phase == PHASE_AG) {
+        acc = load_elem<DT>(rank_ptr(a.bufs, p, owner), i);
+        for (int r = 0; r < p; r++)
+            if (r != owner) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
+        return;
+    }
+    acc = load_elem<DT>(rank_ptr(a.bufs, p, c), i);
+    for (int k = 1; k < p; k++) {
+        int r = c + k;
+        r -= (r >= p) ? p : 0;
+        acc = hop_word<DT, OP>(acc, load_elem<DT>(rank_ptr(a.bufs, p, r), i));
+    }
+    if constexpr (OP == OP_AVG) acc = scale_word<DT>(acc, a.inv_p);
+    if (a.phase == PHASE_RS) {
+        store_elem<DT>(rank_ptr(a.bufs, p, owner), i, acc);
+        return;
+    }
+    for (int r = 0; r < p; r++) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
+}
+
+template <int DT, int OP, int P, int U, bool VEC>
+__global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const __grid_constant__ FusedArgs a) {
+    const int p = P > 0 ? P : a.p;
+    const long long n = a.n;
+    const long long base = n / p, extra = n % p;
+    constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;  // elements per vector
+    const long long nvec = (n + VE - 1) / VE;
+    const long long nfull = n / VE;
+    const long long tv = (long long)blockDim.x * U;
+    for (long long t0 = (long long)blockIdx.x * tv; t0 < nvec; t0 += (long long)gridDim.x * tv) {
+        const long long t1 = t0 + tv < nvec ? t0 + tv : nvec;
+        const int c0 = chunk_of(t0 * VE, base, extra);
+        const long long last = (t1 * VE < n ? t1 * VE : n) - 1;
+        const int c1 = chunk_of(last, base, extra);
+        if (VEC && t1 - t0 == tv && t1 <= nfull && c0 == c1) {
+            fused_fold_vectors<DT, OP, P, U>(a, p, c0, t0 + threadIdx.x, blockDim.x);
+            continue;
+        }
+#pragma unroll 1
+        for (int u = 0; u < U; u++) {
+            const long long v = t0 + threadIdx.x + (long long)u * blockDim.x;
+            if (v >= t1) break;
+            const long long e0 = v * VE;
+            if (VEC && v < nfull) {
+                const int ca = chunk_of(e0, base, extra);
+                const int cb = chunk_of(e0 + VE - 1, base, extra);
+                if (ca == cb) {
+                    fused_fold_vectors<DT, OP, P, 1>(a, p, ca, v, 0);
+                    continue;
+                }
+            }
+            for (int l = 0; l < VE; l++) {
+                const long long i = e0 + l;
+                if (i >= n) break;
+                fused_fold_element<DT, OP>(a, p, chunk_of(i, base, extra), i);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- tree order
+//
+// Tree order over the rank index: adjacent pairs level by level, an odd last
+// entry carried up.  Streaming form: push ranks 0, 1, ... onto a stack and
+// merge the top two while they cover equally many ranks; at the end merge
+// from the top down.  (The two forms build the same tree for every p.)
+// The order does not depend on the chunk, only the reduce-scatter-only
+// phase needs the owner.
+
+template <int DT, int OP, int P>
+__device__ __forceinline__ uint4 tree_fold_vector(const FusedArgs &a, int p, long long v) {
+    constexpr int kMaxDepth = 12;  // log2(RAR_MAX_P) + 2
+    uint4 st[kMaxDepth];
+    int sz[kMaxDepth];
+    int sp = 0;
+    auto push = [&](int r, int pp) {
+        st[sp] = __ldcs(reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, pp, r)) + v);
+        sz[sp] = 1;
+        sp++;
+        while (sp >= 2 && sz[sp - 1] == sz[sp - 2]) {
+            st[sp - 2] = hop_vec<DT, OP>(st[sp - 2], st[sp - 1]);
+            sz[sp - 2] *= 2;
+            sp--;
+        }
+    };
+    if constexpr (P > 0) {
+#pragma unroll
+        for (int r = 0; r < P; r++) push(r, P);
+    } else {
+        for (int r = 0; r < p; r++) push(r, p);
+    }
+    while (sp > 1) {
+        st[sp - 2] = hop_vec<DT, OP>(st[sp - 2], st[sp - 1]);
+        sp--;
+    }
+    return st[0];
+}
+
+template <int DT, int OP, int P>
+__device__ __forceinline__ uint32_t tree_fold_element(const FusedArgs &a, int p, long long i) {
+    constexpr int kMaxDepth = 12;
+    uint32_t st[kMaxDepth];
+    int sz[kMaxDepth];
+    int sp = 0;
+    for (int r = 0; r < p; r++) {
+        st[sp] = load_elem<DT>(rank_ptr(a.bufs, p, r), i);
+        sz[sp] = 1;
+        sp++;
+        while (sp >= 2 && sz[sp - 1] == sz[sp - 2]) {
+            st[sp - 2] = hop_word<DT, OP>(st[sp - 2], st[sp - 1]);
+            sz[sp - 2] *= 2;
+            sp--;
+        }
+    }
+    while (sp > 1) {
+        st[sp - 2] = hop_word<DT, OP>(st[sp - 2], st[sp - 1]);
+        sp--;
+    }
+    return st[0];
+}
+
+template <int DT, int OP, int P, bool VEC>
+__global__ void __launch_bounds__(kFusedThreads) fused_tree_order_kernel(const __grid_constant__ FusedArgs a) {
+    const int p = P > 0 ? P : a.p;
+    const long long n = a.n;
+    const long long base = n / p, extra = n % p;
+    constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
+    const long long nvec = (n + VE - 1) / VE;
+    const long long nfull = n / VE;
+    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (long long)gridDim.x * blockDim.x) {
+        const long long e0 = v * VE;
+        const int ca = chunk_of(e0, base, extra);
+        const int cb = chunk_of((e0 + VE - 1 < n ? e0 + VE - 1 : n - 1), base, extra);
+        if (VEC && v < nfull && (a.phase == PHASE_ALL || ca == cb)) {
+            uint4 acc = tree_fold_vector<DT, OP, P>(a, p, v);
+            if constexpr (OP == OP_AVG) acc = scale_vec<DT>(acc, a.inv_p);
+            if (a.phase == PHASE_RS) {
+                const int owner = (ca == 0) ? p - 1 : ca - 1;
+                __stcs(reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, owner)) + v, acc);
+            } else {
+                for (int r = 0; r < p; r++) __stcs(reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, r)) + v, acc);
+            }
+            continue;
+        }
+        for (int l = 0; l < VE; l++) {
+            const long long i = e0 + l;
+            if (i >= n) break;
+            uint32_t acc = tree_fold_element<DT, OP, P>(a, p, i);
+            if constexpr (OP == OP_AVG) acc = scale_word<DT>(acc, a.inv_p);
+            if (a.phase == PHASE_RS) {
+                const int c = chunk_of(i, base, extra);
+                store_elem<DT>(rank_ptr(a.bufs, p, (c == 0) ? p - 1 : c - 1), i, acc);
+            } else {
+                for (int r = 0; r < p; r++) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- dispatch
+
+template <typename K>
+static int blocks_per_sm_of(K kernel, int threads) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess) return 1;
+    return nb > 0 ? nb : 1;
+}
+
+static int sm_count_cached() {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (sms[dev] == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms[dev] = v > 0 ? v : 1;
+    }
+    return sms[dev];
+}
+
+template <typename K>
+static cudaError_t launch_persistent(K kernel, const FusedArgs &a, long long work_items, int threads,
+                                     int grid_cap, cudaStream_t stream) {
+    const int sms = sm_count_cached();
+    const long long want = (work_items + threads - 1) / threads;
+    long long grid = (long long)sms * blocks_per_sm_of(kernel, threads);
+    if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
+    if (grid > want) grid = want;
+    if (grid < 1) grid = 1;
+    kernel<<<(unsigned)grid, threads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int DT, int OP, int P>
+static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int threads, int grid_cap,
+                                  cudaStream_t stream) {
+    constexpr int VE = 16 / ElemInfo<DT>::bytes;
+    constexpr int U = (P > 0 && P <= 8) ? 2 : 1;
+    if (tree) {
+        if (vec16)
+            return launch_persistent(fused_tree_order_kernel<DT, OP, P, true>, a, (a.n + VE - 1) / VE, threads,
+                                     grid_cap, stream);
+        return launch_persistent(fused_tree_order_kernel<DT, OP, P, false>, a, a.n, threads, grid_cap, stream);
+    }
+    if (vec16)
+        return launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, a, ((a.n + VE - 1) / VE + U - 1) / U,
+                                 threads, grid_cap, stream);
+    return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, false>, a, a.n, threads, grid_cap, stream);
+}
+
+template <int DT, int OP>
+static cudaError_t launch_fused_op(const FusedArgs &a, bool tree, bool vec16, int threads, int grid_cap,
+                                   cudaStream_t stream) {
+    switch (a.p) {
+    case 4: return launch_fused_p<DT, OP, 4>(a, tree, vec16, threads, grid_cap, stream);
+    case 8: return launch_fused_p<DT, OP, 8>(a, tree, vec16, threads, grid_cap, stream);
+    case 16: return launch_fused_p<DT, OP, 16>(a, tree, vec16, threads, grid_cap, stream);
+    default: return launch_fused_p<DT, OP, 0>(a, tree, vec16, threads, grid_cap, stream);
+    }
+}
+
+template <int DT, int OP, int P>
+static int fused_occ_p(bool tree, bool vec16, int threads) {
+    constexpr int U = (P > 0 && P <= 8) ? 2 : 1;
+    if (tree)
+        return vec16 ? blocks_per_sm_of(fused_tree_order_kernel<DT, OP, P, true>, threads)
+                     : blocks_per_sm_of(fused_tree_order_kernel<DT, OP, P, false>, threads);
+    return vec16 ? blocks_per_sm_of(fused_ring_order_kernel<DT, OP, P, U, true>, threads)
+                 : blocks_per_sm_of(fused_ring_order_kernel<DT, OP, P, 1, false>, threads);
+}
+
+template <int DT, int OP>
+static int fused_occ_op(bool tree, bool vec16, int p, int threads) {
+    switch (p) {
+    case 4: return fused_occ_p<DT, OP, 4>(tree, vec16, threads);
+    case 8: return fused_occ_p<DT, OP, 8>(tree, vec16, threads);
+    case 16: return fused_occ_p<DT, OP, 16>(tree, vec16, threads);
+    default: return fused_occ_p<DT, OP, 0>(tree, vec16, threads);
+    }
+}
+
+}  // namespace rar

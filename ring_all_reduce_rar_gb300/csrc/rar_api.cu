@@ -1,0 +1,393 @@
+// rar_api.cu -- the C-ABI of the ring all-reduce library: argument checks,
+// the handle and its scratch, engine planning and launch, status and send
+// accounting.  Declarations and the contract are in include/rar.h.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "rar_internal.h"
+
+namespace {
+
+using namespace rar;
+
+constexpr int kMaxRingCtas = 8192;           // flags / counters capacity
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+constexpr long long kMaxSlicesPerChannelStep = (1ll << 20) - 2;  // progress word field
+
+thread_local std::string g_init_error;  // errors before a handle exists
+
+}  // namespace
+
+struct rar_ctx {
+    int device = 0;
+    rar_options opt{};
+    std::string err;
+    int sm_count = 0;
+    // scratch owned by the handle (ring engines; table for p > kInlineP)
+    unsigned long long *flags = nullptr;
+    unsigned long long *recv_counts = nullptr;
+    RingStatus *status = nullptr;
+    unsigned *abort_word = nullptr;
+    void **ptr_table = nullptr;
+    unsigned epoch = 0;
+    // last call, for rar_status / rar_send_counts
+    bool have_last = false;
+    cudaStream_t last_stream = nullptr;
+    bool last_ring = false;
+    unsigned last_epoch = 0;
+    int last_p = 0;
+    int last_channels = 0;
+    int last_fwd_channels = 0;
+};
+
+namespace {
+
+int fail(rar_ctx *h, int code, const std::string &msg) {
+    if (h) h->err = msg;
+    else g_init_error = msg;
+    return code;
+}
+
+int cuda_fail(rar_ctx *h, cudaError_t e, const char *what) {
+    return fail(h, RAR_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Make `dev` current for the scope of a call and restore the caller's device.
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) {
+            err = cudaSetDevice(dev);
+            changed = err == cudaSuccess;
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+int check_options(rar_ctx *h, const rar_options &o) {
+    if (o.engine < RAR_ENGINE_FUSED || o.engine > RAR_ENGINE_FUSED_TREE)
+        return fail(h, RAR_EINVAL, "unknown engine");
+    if (o.channels < 0 || o.slice_elems < 0 || o.block_threads < 0)
+        return fail(h, RAR_EINVAL, "negative channels, slice_elems or block_threads");
+    if (o.block_threads && (o.block_threads % 32 || o.block_threads > 1024))
+        return fail(h, RAR_EINVAL, "block_threads must be a multiple of 32, at most 1024");
+    if (o.fault_mode < RAR_FAULT_NONE || o.fault_mode > RAR_FAULT_DELAY)
+        return fail(h, RAR_EINVAL, "unknown fault_mode");
+    return RAR_OK;
+}
+
+// Argument checks shared by every collective (include/rar.h, rar_allreduce).
+int check_call(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op) {
+    if (!bufs) return fail(h, RAR_EINVAL, "bufs is NULL");
+    if (p < 1 || p > RAR_MAX_P) return fail(h, RAR_EINVAL, "p must be in [1, RAR_MAX_P]");
+    if (dtype < RAR_INT32 || dtype > RAR_FLOAT16) return fail(h, RAR_EINVAL, "unknown dtype");
+    if (op < RAR_SUM || op > RAR_AVG) return fail(h, RAR_EINVAL, "unknown op");
+    if (op == RAR_AVG && dtype == RAR_INT32) return fail(h, RAR_EUNSUPPORTED, "avg is not offered for int32");
+    const size_t e = (size_t)elem_bytes(dtype);
+    if (n > (size_t)(1ull << 62) / e) return fail(h, RAR_EINVAL, "n * element size overflows");
+    for (int r = 0; r < p; r++)
+        if (!bufs[r]) return fail(h, RAR_EINVAL, "rank buffer " + std::to_string(r) + " is NULL");
+    if (n == 0 || p == 1) return RAR_OK;
+    const size_t bytes = n * e;
+    std::vector<std::pair<uintptr_t, int>> spans;
+    spans.reserve((size_t)p);
+    for (int r = 0; r < p; r++) spans.emplace_back((uintptr_t)bufs[r], r);
+    std::sort(spans.begin(), spans.end());
+    for (int k = 1; k < p; k++)
+        if (spans[k].first < spans[k - 1].first + bytes)
+            return fail(h, RAR_EINVAL, "rank buffers " + std::to_string(spans[k - 1].second) + " and " +
+                                           std::to_string(spans[k].second) + " overlap");
+    if (!h->opt.skip_pointer_check) {
+        for (int r = 0; r < p; r++) {
+            cudaPointerAttributes at{};
+            cudaError_t ce = cudaPointerGetAttributes(&at, bufs[r]);
+            if (ce != cudaSuccess) {
+                cudaGetLastError();
+                return fail(h, RAR_EINVAL, "rank buffer " + std::to_string(r) + " is not CUDA memory");
+            }
+            if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != h->device)
+                return fail(h, RAR_EINVAL, "rank buffer " + std::to_string(r) + " is not device memory of device " +
+                                               std::to_string(h->device));
+        }
+    }
+    return RAR_OK;
+}
+
+// Fill the pointer part of the launch arguments (table copy for large p).
+int fill_ptrs(rar_ctx *h, RankPtrs &rp, void *const *bufs, int p, cudaStream_t stream) {
+    std::memset(&rp, 0, sizeof(rp));
+    if (p <= kInlineP) {
+        for (int r = 0; r < p; r++) rp.inl[r] = bufs[r];
+        return RAR_OK;
+    }
+    // pageable source: staged by the runtime before the call returns
+    cudaError_t ce = cudaMemcpyAsync(h->ptr_table, bufs, sizeof(void *) * (size_t)p, cudaMemcpyHostToDevice, stream);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "copying the rank pointer table");
+    rp.table = h->ptr_table;
+    return RAR_OK;
+}
+
+bool all_aligned16(void *const *bufs, int p) {
+    for (int r = 0; r < p; r++)
+        if ((uintptr_t)bufs[r] % 16) return false;
+    return true;
+}
+
+int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int phase, void *stream_v) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    h->err.clear();
+    int rc = check_call(h, bufs, p, n, dtype, op);
+    if (rc != RAR_OK) return rc;
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    h->have_last = true;
+    h->last_stream = stream;
+    h->last_ring = false;
+    h->last_p = p;
+    if (n == 0 || p == 1) return RAR_OK;
+
+    DeviceGuard dg(h->device);
+    if (dg.err != cudaSuccess) return cuda_fail(h, dg.err, "selecting the device");
+    const bool vec16 = all_aligned16(bufs, p);
+    const float inv_p = 1.0f / (float)p;
+    const int engine = h->opt.engine;
+
+    if (engine == RAR_ENGINE_FUSED || engine == RAR_ENGINE_FUSED_TREE) {
+        FusedArgs a;
+        rc = fill_ptrs(h, a.bufs, bufs, p, stream);
+        if (rc != RAR_OK) return rc;
+        a.n = (long long)n;
+        a.p = p;
+        a.phase = phase;
+        a.inv_p = inv_p;
+        const bool tree = engine == RAR_ENGINE_FUSED_TREE && phase != PHASE_AG;
+        const int threads = 256;  // the fused kernels are compiled for 256 threads
+        cudaError_t ce = launch_fused(a, dtype, op, tree, vec16, threads, 0, stream);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the fused kernel");
+        return RAR_OK;
+    }
+
+    // ---- ring engines
+    const bool bidir = engine == RAR_ENGINE_RING_BIDIR;
+    const int threads = h->opt.block_threads ? h->opt.block_threads : 512;
+    if (threads > 512) return fail(h, RAR_EINVAL, "ring engines run at most 512 threads per CTA");
+    int per_sm = 0;
+    const int max_ctas = std::min(ring_max_coresident_ctas(dtype, op, vec16, threads, &per_sm), kMaxRingCtas);
+    int G = h->opt.channels;
+    if (G == 0) {
+        // about two CTAs per SM in total, at least one (two when bidirectional) per rank
+        G = std::max(1, (2 * h->sm_count) / p);
+    }
+    if (bidir && G < 2) G = 2;
+    if ((long long)G * p > max_ctas) {
+        if (h->opt.channels) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
+        G = max_ctas / p;
+        if (G < (bidir ? 2 : 1))
+            return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
+    }
+    const long long split = bidir ? (long long)n - (long long)n / 2 : (long long)n;  // chunk_bounds(n, 2)
+    const int fwd_channels = bidir ? (G + 1) / 2 : G;
+    long long slice = h->opt.slice_elems ? h->opt.slice_elems : 16384;
+    slice = std::max<long long>(16, (slice + 15) / 16 * 16);
+    {
+        const long long maxchunk = (std::max(split, (long long)n - split) + p - 1) / p;
+        const int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
+        while ((maxchunk + slice - 1) / slice / min_g > kMaxSlicesPerChannelStep) slice *= 2;
+    }
+
+    RingArgs a;
+    rc = fill_ptrs(h, a.bufs, bufs, p, stream);
+    if (rc != RAR_OK) return rc;
+    if (++h->epoch == 0) {
+        // epochs wrapped: clear the progress words once and restart at 1
+        cudaError_t ce = cudaMemsetAsync(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas, stream);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "resetting the progress words");
+        h->epoch = 1;
+    }
+    a.n = (long long)n;
+    a.p = p;
+    a.channels = G;
+    a.fwd_channels = fwd_channels;
+    a.split = split;
+    a.slice = slice;
+    a.first_step = phase == PHASE_AG ? p - 1 : 0;
+    a.n_steps = phase == PHASE_ALL ? 2 * (p - 1) : p - 1;
+    a.inv_p = inv_p;
+    a.epoch = h->epoch;
+    a.flags = h->flags;
+    a.recv_counts = h->recv_counts;
+    a.status = h->status;
+    a.abort_word = h->abort_word;
+    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
+    a.fault_mode = h->opt.fault_mode;
+    a.fault_rank = h->opt.fault_rank;
+    a.fault_delay_ns = h->opt.fault_delay_ns;
+    cudaError_t ce = launch_ring(a, dtype, op, vec16, threads, stream);
+    if (ce != cudaSuccess) {
+        if (ce == cudaErrorCooperativeLaunchTooLarge) {
+            return fail(h, RAR_EUNSUPPORTED, "ring grid cannot be co-resident");
+        }
+        return cuda_fail(h, ce, "launching the ring executor");
+    }
+    h->last_ring = true;
+    h->last_epoch = h->epoch;
+    h->last_channels = G;
+    h->last_fwd_channels = fwd_channels;
+    return RAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rar_version(void) { return RAR_VERSION; }
+
+int rar_init(rar_handle *out, int device, const rar_options *opt) {
+    g_init_error.clear();
+    if (!out) return fail(nullptr, RAR_EINVAL, "out is NULL");
+    *out = nullptr;
+    int ndev = 0;
+    cudaError_t ce = cudaGetDeviceCount(&ndev);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return fail(nullptr, RAR_ECUDA, std::string("cudaGetDeviceCount: ") + cudaGetErrorString(ce));
+    }
+    if (device < 0 || device >= ndev) return fail(nullptr, RAR_EINVAL, "no such device");
+    rar_options o{};
+    if (opt) o = *opt;
+    if (check_options(nullptr, o) != RAR_OK) return RAR_EINVAL;
+
+    rar_ctx *h = new rar_ctx();
+    h->device = device;
+    h->opt = o;
+    DeviceGuard dg(device);
+    if (dg.err != cudaSuccess) {
+        delete h;
+        return fail(nullptr, RAR_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(dg.err));
+    }
+    cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
+    if (h->sm_count < 1) h->sm_count = 1;
+    bool ok = cudaMalloc((void **)&h->flags, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+              cudaMalloc((void **)&h->recv_counts, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+              cudaMalloc((void **)&h->status, sizeof(RingStatus)) == cudaSuccess &&
+              cudaMalloc((void **)&h->abort_word, sizeof(unsigned)) == cudaSuccess &&
+              cudaMalloc((void **)&h->ptr_table, sizeof(void *) * RAR_MAX_P) == cudaSuccess;
+    if (ok) {
+        ok = cudaMemset(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+             cudaMemset(h->recv_counts, 0, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+             cudaMemset(h->status, 0, sizeof(RingStatus)) == cudaSuccess &&
+             cudaMemset(h->abort_word, 0, sizeof(unsigned)) == cudaSuccess &&
+             cudaDeviceSynchronize() == cudaSuccess;
+    }
+    if (!ok) {
+        cudaGetLastError();
+        cudaFree(h->flags);
+        cudaFree(h->recv_counts);
+        cudaFree(h->status);
+        cudaFree(h->abort_word);
+        cudaFree(h->ptr_table);
+        delete h;
+        return fail(nullptr, RAR_ENOMEM, "allocating the handle's scratch failed");
+    }
+    *out = h;
+    return RAR_OK;
+}
+
+int rar_set_options(rar_handle h, const rar_options *opt) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    rar_options o{};
+    if (opt) o = *opt;
+    int rc = check_options(h, o);
+    if (rc != RAR_OK) return rc;
+    h->opt = o;
+    return RAR_OK;
+}
+
+int rar_allreduce(rar_handle h, void *const *bufs, int p, size_t n, int dtype, int op, void *stream) {
+    return run(h, bufs, p, n, dtype, op, PHASE_ALL, stream);
+}
+
+int rar_reduce_scatter(rar_handle h, void *const *bufs, int p, size_t n, int dtype, int op, void *stream) {
+    return run(h, bufs, p, n, dtype, op, PHASE_RS, stream);
+}
+
+int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, void *stream) {
+    return run(h, bufs, p, n, dtype, RAR_SUM, PHASE_AG, stream);
+}
+
+int rar_status(rar_handle h) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    if (!h->have_last) return RAR_OK;
+    DeviceGuard dg(h->device);
+    cudaError_t ce = cudaStreamSynchronize(h->last_stream);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "synchronising the last call's stream");
+    if (!h->last_ring) return RAR_OK;
+    RingStatus st{};
+    ce = cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the status word");
+    if (st.epoch == h->last_epoch && st.code != 0) {
+        char buf[256];
+        std::snprintf(buf, sizeof(buf),
+                      "ring wait timed out: rank %d, step %d, slice %d, waiting on rank %d "
+                      "(progress word 0x%llx, wanted 0x%llx)",
+                      st.rank, st.step, st.slice, st.waited_on, st.flag_seen, st.flag_wanted);
+        h->err = buf;
+        return (int)st.code;
+    }
+    return RAR_OK;
+}
+
+int rar_send_counts(rar_handle h, unsigned long long *out, int p) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    if (!out) return fail(h, RAR_EINVAL, "out is NULL");
+    if (!h->have_last || p != h->last_p) return fail(h, RAR_EINVAL, "p differs from the last call's p");
+    for (int r = 0; r < p; r++) out[r] = 0;
+    int rc = rar_status(h);
+    if (rc != RAR_OK && rc != RAR_ETIMEOUT) return rc;
+    if (!h->last_ring) return RAR_OK;
+    const int G = h->last_channels;
+    std::vector<unsigned long long> rc_counts((size_t)p * (size_t)G);
+    DeviceGuard dg(h->device);
+    cudaError_t ce = cudaMemcpy(rc_counts.data(), h->recv_counts, sizeof(unsigned long long) * rc_counts.size(),
+                                cudaMemcpyDeviceToHost);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the send counters");
+    // a CTA counts what it received; the sender is its left (forward ring)
+    // or right (mirrored ring) neighbour
+    for (int r = 0; r < p; r++)
+        for (int j = 0; j < G; j++) {
+            const bool fwd = j < h->last_fwd_channels;
+            const int sender = fwd ? (r + p - 1) % p : (r + 1) % p;
+            out[sender] += rc_counts[(size_t)r * G + j];
+        }
+    return RAR_OK;
+}
+
+const char *rar_last_error(rar_handle h) {
+    if (!h) return g_init_error.c_str();
+    return h->err.c_str();
+}
+
+int rar_destroy(rar_handle h) {
+    if (!h) return RAR_OK;
+    {
+        DeviceGuard dg(h->device);
+        if (h->have_last) cudaStreamSynchronize(h->last_stream);
+        cudaFree(h->flags);
+        cudaFree(h->recv_counts);
+        cudaFree(h->status);
+        cudaFree(h->abort_word);
+        cudaFree(h->ptr_table);
+    }
+    delete h;
+    return RAR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// rar_internal.h -- launch arguments shared by the host runtime and the
+// kernels of the ring all-reduce library.  Not a public header.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rar.h"
+
+namespace rar {
+
+// Rank pointers travel in the kernel parameters for p <= kInlineP; larger p
+// read a device-side table kept in the handle's scratch.
+constexpr int kInlineP = 64;
+
+enum Dtype { DT_I32 = RAR_INT32, DT_F32 = RAR_FLOAT32, DT_BF16 = RAR_BFLOAT16, DT_F16 = RAR_FLOAT16 };
+enum Op { OP_SUM = RAR_SUM, OP_MAX = RAR_MAX, OP_AVG = RAR_AVG };
+
+// Which part of the schedule a launch runs.
+enum Phase { PHASE_ALL = 0, PHASE_RS = 1, PHASE_AG = 2 };
+
+inline int elem_bytes(int dt) { return (dt == DT_BF16 || dt == DT_F16) ? 2 : 4; }
+
+struct RankPtrs {
+    void *inl[kInlineP];
+    void *const *table;  // device array of p pointers when p > kInlineP
+};
+
+// Fused engines: one launch covers [0, n) of every rank.
+struct FusedArgs {
+    RankPtrs bufs;
+    long long n;
+    int p;
+    int phase;     // Phase
+    float inv_p;   // binary32 nearest to 1/p
+};
+
+// Device-side status of a ring launch (written by the first CTA that gives up).
+struct RingStatus {
+    unsigned epoch;   // epoch of the call that failed (0: none yet)
+    unsigned code;    // RAR_ETIMEOUT
+    int rank;         // rank whose wait ran out
+    int step;         // global schedule step it was waiting to start
+    int slice;        // slice index within the chunk
+    int waited_on;    // neighbour rank it was waiting for
+    unsigned long long flag_seen;
+    unsigned long long flag_wanted;
+};
+
+// Ring engines: persistent cooperative launch of p * channels CTAs.
+struct RingArgs {
+    RankPtrs bufs;
+    long long n;
+    int p;
+    int channels;        // CTAs per rank
+    int fwd_channels;    // bidirectional: channels [0, fwd_channels) run the
+                         // forward ring on the first half, the rest the
+                         // mirrored ring on the second half; == channels if
+                         // not bidirectional
+    long long split;     // bidirectional: first index of the second half (n otherwise)
+    long long slice;     // elements per slice
+    int first_step;      // global schedule steps [first_step, first_step + n_steps)
+    int n_steps;
+    float inv_p;
+    unsigned epoch;
+    unsigned long long *flags;        // [p * channels] progress words
+    unsigned long long *recv_counts;  // [p * channels] elements received by each CTA
+    RingStatus *status;
+    unsigned *abort_word;             // == epoch once any CTA gave up
+    unsigned long long timeout_ns;
+    int fault_mode;
+    int fault_rank;
+    unsigned fault_delay_ns;
+};
+
+// Launchers (return cudaError_t of the launch).  `vec16` selects the 128-bit
+// path (all rank pointers 16-byte aligned).
+cudaError_t launch_fused(const FusedArgs &a, int dtype, int op, bool tree, bool vec16,
+                         int threads, int grid_cap, cudaStream_t stream);
+cudaError_t launch_ring(const RingArgs &a, int dtype, int op, bool vec16, int threads,
+                        cudaStream_t stream);
+// Largest co-resident grid for the ring kernel of this dtype/op (per device).
+int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
+// Co-resident CTAs per SM for a fused kernel instance.
+int fused_blocks_per_sm(int dtype, int op, bool tree, bool vec16, int p, int threads);
+
+}  // namespace rar

@@ -1,0 +1,306 @@
+// ring.cu -- engine (b): the schedule-faithful persistent ring executor.
+//
+// The schedule of "Ring All-Reduce, in depth" ("The schedule"), run as
+// written: p rank groups of `channels` CTAs each, all co-resident (one
+// cooperative launch).  At reduce-scatter step s rank r receives chunk
+// (r - 1 - s) mod p from rank r - 1 and combines it into its own copy; at
+// all-gather step s it receives chunk (r - s) mod p and overwrites its copy.
+// Data moves through the rank buffers themselves (the receiver reads the
+// sender's copy in place), so a reduce-scatter hop costs 3 element moves
+// (read incoming, read own, write own) and an all-gather hop 2.
+//
+// Pipelining ("What real libraries add", "Pipelining"): each chunk is cut
+// into slices of `slice` elements; slice k belongs to channel k mod
+// channels, and every channel is an independent ring over its slices
+// ("Multiple rings, or channels").  A CTA publishes its progress after each
+// slice with a release store of a 64-bit word
+//     (epoch << 32) | (step << 20) | (slice-within-channel + 1),
+// and the right neighbour's CTA of the same channel acquires it before it
+// reads that slice at the next step.  Epoch-tagged words need no reset
+// between calls.
+//
+// In-place safety: rank r - 1 overwrites the chunk r read at reduce-scatter
+// step s only at its all-gather step s, and that write waits on a chain of
+// flags that starts with r's own release after the read (the chunk's
+// remaining reduce-scatter hops, its owner, the all-gather hops up to r - 1).
+//
+// Bidirectional variant ("Bidirectional rings"): channels
+// [fwd_channels, channels) run the mirrored ring (send to r - 1) on the
+// second half of the buffer, cut by chunk_bounds(n, 2).
+//
+// Every wait is bounded (globaltimer and an iteration cap).  A CTA that runs
+// out records the failure in the status word, raises the abort word and
+// returns; the others see the abort word in their next wait and return.
+// Nothing traps or spins forever.
+#include "elem_ops.cuh"
+
+namespace rar {
+
+constexpr int kRingThreads = 512;
+constexpr int kRingUnroll = 4;
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned long long progress_tag(unsigned epoch, int step, long long loc) {
+    return ((unsigned long long)epoch << 32) | ((unsigned long long)step << 20) | (unsigned long long)(loc + 1);
+}
+
+__device__ __forceinline__ int mod_p(int v, int p) {
+    v %= p;
+    return v < 0 ? v + p : v;
+}
+
+// Record a timeout (first CTA of this call only) and raise the abort word.
+__device__ void ring_give_up(const RingArgs &a, int rank, int step, long long slice, int nb,
+                             unsigned long long seen, unsigned long long wanted) {
+    unsigned prev = atomicMax(&a.status->epoch, a.epoch);
+    if (prev < a.epoch) {
+        a.status->code = RAR_ETIMEOUT;
+        a.status->rank = rank;
+        a.status->step = step;
+        a.status->slice = (int)slice;
+        a.status->waited_on = nb;
+        a.status->flag_seen = seen;
+        a.status->flag_wanted = wanted;
+        __threadfence();
+    }
+    atomicMax(a.abort_word, a.epoch);
+}
+
+// Bounded acquire-wait for the neighbour's progress word.  Returns false if
+// the wait ran out or another CTA aborted the call.
+__device__ bool ring_wait(const RingArgs &a, const unsigned long long *flag, unsigned long long target, int rank,
+                          int step, long long slice, int nb) {
+    unsigned long long v = ld_acquire_u64(flag);
+    if (v >= target) return true;
+    const unsigned long long t0 = global_ns();
+    const unsigned long long max_iters = a.timeout_ns / 16ull + (1ull << 20);
+    for (unsigned long long it = 0;; it++) {
+        __nanosleep(32);
+        v = ld_acquire_u64(flag);
+        if (v >= target) return true;
+        if (ld_relaxed_u32(a.abort_word) == a.epoch) return false;
+        if (it >= max_iters || global_ns() - t0 > a.timeout_ns) {
+            ring_give_up(a, rank, step, slice, nb, v, target);
+            return false;
+        }
+    }
+}
+
+// Injected straggler: pause about `ns` (bounded by the same clock).
+__device__ void ring_delay(unsigned ns) {
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < (1 << 22) && global_ns() - t0 < ns; it++) __nanosleep(256);
+}
+
+// One slice [lo, hi) of one hop: dst = reduce ? op(src, dst) : src, then the
+// owner's avg scaling if `scale`.
+template <int DT, int OP, bool VEC>
+__device__ __forceinline__ void ring_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
+                                           bool scale, float inv_p) {
+    constexpr int hop_op = OP == OP_AVG ? OP_SUM : OP;
+    constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
+    const int T = blockDim.x;
+    long long vlo = (lo + VE - 1) / VE, vhi = hi / VE;
+    if (!VEC || vlo >= vhi) vlo = vhi = lo / VE;  // all of it on the element path
+    const long long elo = VEC ? vlo * VE : lo;      // [lo, elo) and [ehi, hi) per element
+    const long long ehi = VEC ? vhi * VE : lo;
+    auto one = [&](long long i) {
+        uint32_t x = load_elem<DT>(src, i);
+        if (reduce) x = hop_word<DT, hop_op>(x, load_elem<DT>(dst, i));
+        if (OP == OP_AVG && scale) x = scale_word<DT>(x, inv_p);
+        store_elem<DT>(dst, i, x);
+    };
+    if constexpr (!VEC) {
+        for (long long i = lo + threadIdx.x; i < hi; i += T) one(i);
+        return;
+    }
+    if (vlo == vhi) {
+        for (long long i = lo + threadIdx.x; i < hi; i += T) one(i);
+        return;
+    }
+    for (long long i = lo + threadIdx.x; i < elo; i += T) one(i);
+    for (long long i = ehi + threadIdx.x; i < hi; i += T) one(i);
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    for (long long v = vlo + threadIdx.x; v < vhi; v += (long long)T * kRingUnroll) {
+        uint4 in[kRingUnroll], own[kRingUnroll];
+#pragma unroll
+        for (int u = 0; u < kRingUnroll; u++) {
+            const long long vv = v + (long long)u * T;
+            if (vv < vhi) {
+                in[u] = __ldcg(s4 + vv);
+                if (reduce) own[u] = __ldcs(d4 + vv);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRingUnroll; u++) {
+            const long long vv = v + (long long)u * T;
+            if (vv < vhi) {
+                uint4 x = in[u];
+                if (reduce) x = hop_vec<DT, hop_op>(x, own[u]);
+                if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
+                d4[vv] = x;
+            }
+        }
+    }
+}
+
+template <int DT, int OP, bool VEC>
+__global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __grid_constant__ RingArgs a) {
+    __shared__ int s_stop;
+    const int p = a.p;
+    const int r = blockIdx.x / a.channels;
+    const int j = blockIdx.x % a.channels;
+    const bool fwd = j < a.fwd_channels;
+    const int jj = fwd ? j : j - a.fwd_channels;
+    const int GG = fwd ? a.fwd_channels : a.channels - a.fwd_channels;
+    const long long seg_lo = fwd ? 0 : a.split;
+    const long long L = fwd ? a.split : a.n - a.split;
+    const int nb = fwd ? mod_p(r - 1, p) : mod_p(r + 1, p);  // the rank this CTA receives from
+    const char *src = rank_ptr(a.bufs, p, nb);
+    char *dst = rank_ptr(a.bufs, p, r);
+    unsigned long long *my_flag = a.flags + blockIdx.x;
+    const unsigned long long *nb_flag = a.flags + (long long)nb * a.channels + j;
+    const long long base = L / p, extra = L % p;
+    unsigned long long received = 0;
+    const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
+    const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
+
+    if (!muted) {
+        for (int step = a.first_step; step < a.first_step + a.n_steps; step++) {
+            const bool rs = step < p - 1;
+            const int s = rs ? step : step - (p - 1);
+            int c;
+            if (fwd) c = rs ? mod_p(r - 1 - s, p) : mod_p(r - s, p);
+            else c = rs ? mod_p(r + 1 + s, p) : mod_p(r + s, p);
+            const long long cs = seg_lo + chunk_start(c, base, extra);
+            const long long ce = seg_lo + chunk_start(c + 1, base, extra);
+            const long long nsl = (ce - cs + a.slice - 1) / a.slice;
+            const bool scale = rs && s == p - 2;  // this rank becomes the chunk's owner
+            long long loc = 0;
+            for (long long sl = jj; sl < nsl; sl += GG, loc++) {
+                if (threadIdx.x == 0) {
+                    bool ok;
+                    if (step > a.first_step)
+                        ok = ring_wait(a, nb_flag, progress_tag(a.epoch, step - 1, loc), r, step, sl, nb);
+                    else
+                        ok = ld_relaxed_u32(a.abort_word) != a.epoch;
+                    if (ok && slow) ring_delay(a.fault_delay_ns);
+                    s_stop = ok ? 0 : 1;
+                }
+                __syncthreads();
+                if (s_stop) goto done;
+                {
+                    const long long lo = cs + sl * a.slice;
+                    const long long hi = lo + a.slice < ce ? lo + a.slice : ce;
+                    ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale, a.inv_p);
+                    received += (unsigned long long)(hi - lo);
+                }
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    st_release_u64(my_flag, progress_tag(a.epoch, step, loc));
+                }
+            }
+        }
+    }
+done:
+    if (threadIdx.x == 0) a.recv_counts[blockIdx.x] = received;
+}
+
+template <int DT, int OP, bool VEC>
+static cudaError_t launch_ring_t(const RingArgs &a, int threads, cudaStream_t stream) {
+    void *args[] = {const_cast<RingArgs *>(&a)};
+    return cudaLaunchCooperativeKernel((const void *)ring_executor_kernel<DT, OP, VEC>,
+                                       dim3((unsigned)(a.p * a.channels)), dim3((unsigned)threads), args, 0, stream);
+}
+
+template <int DT, int OP>
+static cudaError_t launch_ring_op(const RingArgs &a, bool vec16, int threads, cudaStream_t stream) {
+    return vec16 ? launch_ring_t<DT, OP, true>(a, threads, stream) : launch_ring_t<DT, OP, false>(a, threads, stream);
+}
+
+cudaError_t launch_ring(const RingArgs &a, int dtype, int op, bool vec16, int threads, cudaStream_t stream) {
+    switch (dtype) {
+    case DT_I32:
+        if (op == OP_SUM) return launch_ring_op<DT_I32, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_ring_op<DT_I32, OP_MAX>(a, vec16, threads, stream);
+        break;
+    case DT_F32:
+        if (op == OP_SUM) return launch_ring_op<DT_F32, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_ring_op<DT_F32, OP_MAX>(a, vec16, threads, stream);
+        if (op == OP_AVG) return launch_ring_op<DT_F32, OP_AVG>(a, vec16, threads, stream);
+        break;
+    case DT_BF16:
+        if (op == OP_SUM) return launch_ring_op<DT_BF16, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_ring_op<DT_BF16, OP_MAX>(a, vec16, threads, stream);
+        if (op == OP_AVG) return launch_ring_op<DT_BF16, OP_AVG>(a, vec16, threads, stream);
+        break;
+    case DT_F16:
+        if (op == OP_SUM) return launch_ring_op<DT_F16, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_ring_op<DT_F16, OP_MAX>(a, vec16, threads, stream);
+        if (op == OP_AVG) return launch_ring_op<DT_F16, OP_AVG>(a, vec16, threads, stream);
+        break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename K>
+static int occ_of(K kernel, int threads) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess) return 0;
+    return nb;
+}
+
+template <int DT, int OP>
+static int ring_occ(bool vec16, int threads) {
+    return vec16 ? occ_of(ring_executor_kernel<DT, OP, true>, threads)
+                 : occ_of(ring_executor_kernel<DT, OP, false>, threads);
+}
+
+int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm) {
+    int per_sm = 0;
+    switch (dtype) {
+    case DT_I32: per_sm = op == OP_SUM ? ring_occ<DT_I32, OP_SUM>(vec16, threads) : ring_occ<DT_I32, OP_MAX>(vec16, threads); break;
+    case DT_F32:
+        per_sm = op == OP_SUM ? ring_occ<DT_F32, OP_SUM>(vec16, threads)
+                 : op == OP_MAX ? ring_occ<DT_F32, OP_MAX>(vec16, threads)
+                                : ring_occ<DT_F32, OP_AVG>(vec16, threads);
+        break;
+    case DT_BF16:
+        per_sm = op == OP_SUM ? ring_occ<DT_BF16, OP_SUM>(vec16, threads)
+                 : op == OP_MAX ? ring_occ<DT_BF16, OP_MAX>(vec16, threads)
+                                : ring_occ<DT_BF16, OP_AVG>(vec16, threads);
+        break;
+    default:
+        per_sm = op == OP_SUM ? ring_occ<DT_F16, OP_SUM>(vec16, threads)
+                 : op == OP_MAX ? ring_occ<DT_F16, OP_MAX>(vec16, threads)
+                                : ring_occ<DT_F16, OP_AVG>(vec16, threads);
+        break;
+    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (out_per_sm) *out_per_sm = per_sm;
+    return per_sm * sms;
+}
+
+}  // namespace rar

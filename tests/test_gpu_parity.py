@@ -1,0 +1,411 @@
+"""GPU parity: every engine against the oracle, through the C-ABI.
+
+Bit-exact for every ring-order path (int32, fp32, bf16, f16, sum/max/avg);
+the tree-order engine is bit-exact against the oracle's tree fold and within
+4 p 2^-24 sum|x| of the fp64 sum.  Inputs come from workloads/ (seeded),
+generated on the CPU and uploaded, except the 16 GiB workload, which is
+generated on the GPU by the same generator and checked against a CPU
+regeneration at the sampled indices."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as w
+
+pytestmark = pytest.mark.gpu
+
+RING_ENGINES = ["fused", "ring", "ring_bidir"]
+
+
+@pytest.fixture(scope="module")
+def rar():
+    import ring_all_reduce_rar_gb300 as rar
+    rar.build()
+    rar.load_library()
+    assert torch.cuda.is_available()
+    return rar
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return torch.device("cuda:0")
+
+
+def upload(host_rows, dev, offset_elems=0):
+    """Copy CPU rows into one padded device allocation (optionally offset to
+    break 16-byte alignment); returns (storage, rows)."""
+    p, n = len(host_rows), host_rows[0].numel()
+    dtype = {torch.int32: "int32", torch.float32: "float32", torch.bfloat16: "bfloat16",
+             torch.float16: "float16"}[host_rows[0].dtype]
+    big, _ = w.alloc_ranks(p, n + offset_elems, dtype, dev)
+    rows = [big[r, offset_elems:offset_elems + n] for r in range(p)]
+    for r in range(p):
+        rows[r].copy_(host_rows[r])
+    return big, rows
+
+
+def oracle_expect(host_rows, dtype, op, engine):
+    ref = [w.to_storage_numpy(t).copy() for t in host_rows]
+    if engine == "ring_bidir":
+        sends = oracle.simulate_bidir(ref, dtype, op)
+    elif engine == "fused_tree":
+        oracle.tree_fold(ref, dtype, op)
+        sends = None
+    else:
+        sends = oracle.simulate(ref, dtype, op)
+    return ref, sends
+
+
+def assert_bits_equal(rows, ref, what=""):
+    for r, (t, e) in enumerate(zip(rows, ref)):
+        got = w.to_storage_numpy(t)
+        if not np.array_equal(got.view(np.uint8), e.view(np.uint8)):
+            bad = np.nonzero(got.view(e.dtype) != e)[0]
+            raise AssertionError(f"{what}: rank {r} differs at {len(bad)} elements, first {bad[:8]}")
+
+
+def run_case(rar, dev, host_rows, dtype, op, engine, offset=0, **opts):
+    ref, sends = oracle_expect(host_rows, dtype, op, engine)
+    _, rows = upload(host_rows, dev, offset)
+    with rar.Handle(0, engine=engine, **opts) as h:
+        h.allreduce(rows, op=op)
+        h.check()
+        got_sends = h.send_counts(len(rows))
+    torch.cuda.synchronize()
+    assert_bits_equal(rows, ref, f"{engine} {dtype} {op} p={len(rows)} n={rows[0].numel()}")
+    if engine in ("ring", "ring_bidir"):
+        assert list(got_sends) == list(sends)
+    else:
+        assert list(got_sends) == [0] * len(rows)
+
+
+def gen(p, n, dtype, dist, seed):
+    _, rows = w.make_inputs(p, n, dtype, dist, seed)
+    return rows
+
+
+# ----------------------------------------------------------------- page cases
+
+@pytest.mark.parametrize("engine", RING_ENGINES + ["fused_tree"])
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+def test_page_trace_p4_n4(rar, dev, engine, dtype):
+    """"Ring All-Reduce, in depth", "Tracing four GPUs": [10, 100, 1000, 10000]
+    on every rank, six elements sent per rank."""
+    vals = w.page_trace_inputs()
+    host = [torch.tensor(v, dtype=torch.float32).to(w.TORCH_DTYPES[dtype]) for v in vals]
+    _, rows = upload(host, dev)
+    with rar.Handle(0, engine=engine) as h:
+        h.allreduce(rows)
+        h.check()
+        sends = h.send_counts(4)
+    for t in rows:
+        assert t.float().tolist() == [10.0, 100.0, 1000.0, 10000.0]
+    if engine == "ring":
+        assert sends == [6, 6, 6, 6]
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_semantics_example_p4_n1(rar, dev, engine):
+    """"AllReduce 与 Ring 通信算法详解": [1, 2, 3, 4] -> 10 everywhere (N < p)."""
+    host = [torch.tensor([float(r + 1)]) for r in range(4)]
+    _, rows = upload(host, dev)
+    with rar.Handle(0, engine=engine) as h:
+        h.allreduce(rows)
+        h.check()
+        sends = h.send_counts(4)
+    assert [t.item() for t in rows] == [10.0] * 4
+    if engine == "ring":
+        assert sends == [2, 2, 1, 1]
+
+
+# ----------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_p4_n4099_f32_uniform_sum(rar, dev, engine):
+    cfg = w.WORKLOADS["p4_n4099_f32"]
+    host = gen(cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"]))
+    run_case(rar, dev, host, "float32", "sum", engine)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("op", ["sum", "avg"])
+def test_p8_n6553600_f32_normal(rar, dev, engine, op):
+    cfg = w.WORKLOADS["p8_n6553600_f32"]
+    host = gen(cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"]))
+    run_case(rar, dev, host, "float32", op, engine)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_p64_bf16_full_compare_reduced_n(rar, dev, engine):
+    """p = 64 bf16 (large-p case) at a size the oracle runs element by
+    element: 64 chunks of ~1000 elements plus a ragged tail."""
+    host = gen(64, 64 * 1000 + 13, "bfloat16", ("normal", 1e-2), w.seed_of(3))
+    run_case(rar, dev, host, "bfloat16", "sum", engine)
+
+
+def sampled_indices(n, p, m, seed, halves=False):
+    g = np.random.default_rng(seed)
+    idx = set(g.integers(0, n, size=m).tolist())
+    segs = [(0, n)]
+    if halves:
+        h = n - n // 2
+        segs = [(0, h), (h, n)]
+    for lo, hi in segs:
+        for c, (s, e) in enumerate(oracle.chunk_bounds(hi - lo, p)):
+            for i in (s - 1, s, s + 1, e - 2, e - 1):
+                if lo <= lo + i < hi:
+                    idx.add(lo + i)
+    idx.update([0, n - 1])
+    return np.array(sorted(i for i in idx if 0 <= i < n), dtype=np.int64)
+
+
+def check_sampled(rows, p, n, dtype, dist, seed, op, engine, m=200_000):
+    """Sampled parity at full size: the oracle's per-element fold on inputs
+    regenerated on the CPU at the sampled indices."""
+    mode = {"ring_bidir": "bidir", "fused_tree": "tree"}.get(engine, "ring")
+    idx = sampled_indices(n, p, m, seed, halves=(engine == "ring_bidir"))
+    vals = w.sample_inputs(seed, p, torch.from_numpy(idx), dist, dtype)
+    vals_np = np.stack([w.to_storage_numpy(vals[r]) for r in range(p)])
+    expect = oracle.fold_sampled(vals_np, idx, n, dtype, op, mode)
+    ti = torch.from_numpy(idx).to(rows[0].device)
+    for r in range(p):
+        got = w.to_storage_numpy(rows[r][ti])
+        assert np.array_equal(got.view(np.uint8), expect.view(np.uint8)), f"{engine} rank {r}"
+    for r in range(1, p):
+        assert torch.equal(rows[r], rows[0]), f"{engine}: rank {r} differs from rank 0"
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_p64_n16777216_bf16_full_size_sampled(rar, dev, engine):
+    cfg = w.WORKLOADS["p64_n16777216_bf16"]
+    p, n, seed = cfg["p"], cfg["n"], w.seed_of(cfg["index"])
+    big, rows = w.make_inputs(p, n, cfg["dtype"], cfg["dist"], seed, device=dev)
+    with rar.Handle(0, engine=engine) as h:
+        h.allreduce(rows)
+        h.check()
+    check_sampled(rows, p, n, cfg["dtype"], cfg["dist"], seed, "sum", engine)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_p8_n2pow30_bf16_full_size_sampled(rar, dev, engine):
+    """The 16 GiB workload, in the launch configuration the benchmark times."""
+    cfg = w.WORKLOADS["p8_n1073741824_bf16"]
+    p, n, seed = cfg["p"], cfg["n"], w.seed_of(cfg["index"])
+    big, rows = w.make_inputs(p, n, cfg["dtype"], cfg["dist"], seed, device=dev)
+    # the GPU-side generation equals the CPU generator at sampled indices
+    idx = torch.from_numpy(sampled_indices(n, p, 10_000, 1))
+    cpu = w.sample_inputs(seed, p, idx, cfg["dist"], cfg["dtype"])
+    for r in range(p):
+        assert torch.equal(rows[r][idx.to(dev)].cpu(), cpu[r])
+    with rar.Handle(0, engine=engine) as h:
+        h.allreduce(rows)
+        h.check()
+    check_sampled(rows, p, n, cfg["dtype"], cfg["dist"], seed, "sum", engine)
+    del big
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("pair", range(3))
+def test_p16_sweep(rar, dev, engine, pair):
+    """p = 16, N = 4^5 .. 4^13: int32 sum, fp32 max, fp32 avg.  Element by
+    element up to 4^10, sampled above."""
+    dtype, op, dist = w.SWEEP_PAIRS[pair]
+    seed = w.seed_of(w.SWEEP_INDEX) + 16 * pair
+    p = w.SWEEP_P
+    for n in w.SWEEP_SIZES:
+        if n <= 4 ** 10:
+            host = gen(p, n, dtype, dist, seed)
+            run_case(rar, dev, host, dtype, op, engine)
+        else:
+            big, rows = w.make_inputs(p, n, dtype, dist, seed, device=dev)
+            with rar.Handle(0, engine=engine) as h:
+                h.allreduce(rows, op=op)
+                h.check()
+            check_sampled(rows, p, n, dtype, dist, seed, op, engine, m=50_000)
+
+
+# ----------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_odd_p_ragged_n_and_small_n(rar, dev, engine):
+    """Runtime-p paths (p not 4/8/16), N < p (empty chunks), ragged tails."""
+    for p in [2, 3, 5, 7, 13, 31]:
+        for n in [1, 2, p - 1, p, p + 1, 8 * p + 3, 1000 + p]:
+            if n < 1:
+                continue
+            host = gen(p, n, "float32", ("normal", 1.0), 1000 * p + n)
+            run_case(rar, dev, host, "float32", "sum", engine)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("dtype,op", [("int32", "max"), ("bfloat16", "max"), ("bfloat16", "avg"),
+                                      ("float16", "sum"), ("float16", "avg"), ("float16", "max"),
+                                      ("int32", "sum"), ("float32", "max")])
+def test_dtype_op_matrix(rar, dev, engine, dtype, op):
+    dist = ("uniform_int", -(1 << 20), 21) if dtype == "int32" else ("normal", 1.0)
+    for p, n in [(4, 4099), (8, 8 * 777 + 5), (6, 1001)]:
+        host = gen(p, n, dtype, dist, 7 * p + n)
+        run_case(rar, dev, host, dtype, op, engine)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_misaligned_pointers_take_element_path(rar, dev, engine):
+    """Rank pointers offset by one element (not 16-byte aligned): same bits."""
+    for dtype in ["float32", "bfloat16"]:
+        host = gen(8, 8 * 513 + 3, dtype, ("normal", 1.0), 5)
+        run_case(rar, dev, host, dtype, "sum", engine, offset=1)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_large_p_uses_pointer_table(rar, dev, engine):
+    """p > 64: rank pointers travel through the device-side table."""
+    p = 96 if engine == "fused" else 72
+    host = gen(p, p * 50 + 7, "float32", ("normal", 1.0), 11)
+    run_case(rar, dev, host, "float32", "sum", engine)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES)
+def test_trivial_calls(rar, dev, engine):
+    one = [torch.arange(10, dtype=torch.float32, device=dev)]
+    empty = [torch.zeros(0, device=dev) for _ in range(4)]
+    with rar.Handle(0, engine=engine) as h:
+        h.allreduce(one)
+        h.allreduce(empty)
+        h.check()
+    assert one[0].tolist() == list(map(float, range(10)))
+
+
+def test_fp32_special_values(rar, dev):
+    """Subnormals survive (no flush to zero), overflow goes to inf, -0 kept."""
+    tiny = np.float32(1e-45)
+    host = [torch.tensor([tiny, 3e38, -0.0, 1.0] * 8, dtype=torch.float32) for _ in range(4)]
+    for engine in RING_ENGINES:
+        run_case(rar, dev, host, "float32", "sum", engine)
+
+
+def test_bf16_subnormals_and_ties(rar, dev):
+    vals = np.array([0x0001, 0x0080, 0x8001, 0x3F80, 0x3B80, 0x4380, 0x7F7F] * 9, dtype=np.uint16)
+    host = [torch.from_numpy(np.roll(vals, r).astype(np.int16)).view(torch.bfloat16) for r in range(5)]
+    for engine in RING_ENGINES:
+        run_case(rar, dev, host, "bfloat16", "sum", engine)
+
+
+# ----------------------------------------------------------------- ring engine specifics
+
+def test_ring_race_check_slices_and_channels(rar, dev):
+    """Results must not depend on slice size, channel count or block size."""
+    host = gen(8, 8 * 10000 + 5, "bfloat16", ("normal", 1e-2), 21)
+    ref, _ = oracle_expect(host, "bfloat16", "sum", "ring")
+    for engine in ["ring", "ring_bidir"]:
+        r2 = oracle_expect(host, "bfloat16", "sum", engine)[0]
+        for ch, sl, bt in [(1, 16, 128), (2, 64, 256), (3, 1024, 512), (7, 4096, 512), (16, 160, 64)]:
+            _, rows = upload(host, dev)
+            with rar.Handle(0, engine=engine, channels=ch, slice_elems=sl, block_threads=bt) as h:
+                h.allreduce(rows)
+                h.check()
+            assert_bits_equal(rows, r2 if engine == "ring_bidir" else ref, f"{engine} ch={ch} sl={sl}")
+
+
+def test_ring_back_to_back_calls_reuse_flags(rar, dev):
+    host = gen(4, 4099, "float32", ("uniform", -1.0, 1.0), 3)
+    ref, _ = oracle_expect(host, "float32", "sum", "ring")
+    with rar.Handle(0, engine="ring") as h:
+        for _ in range(5):
+            _, rows = upload(host, dev)
+            h.allreduce(rows)
+            h.check()
+            assert_bits_equal(rows, ref, "repeat")
+
+
+@pytest.mark.parametrize("engine", ["ring", "ring_bidir"])
+def test_ring_muted_rank_times_out_and_handle_recovers(rar, dev, engine):
+    """A rank that never publishes: its neighbour's bounded wait runs out,
+    the call reports RAR_ETIMEOUT, and the next call on the same handle
+    succeeds (the context stays usable)."""
+    host = gen(4, 4 * 4096, "float32", ("normal", 1.0), 9)
+    _, rows = upload(host, dev)
+    with rar.Handle(0, engine=engine, timeout_ns=50_000_000, fault_mode="mute", fault_rank=2,
+                    slice_elems=512) as h:
+        h.allreduce(rows)
+        assert h.status() == 5  # RAR_ETIMEOUT
+        assert "timed out" in rar.rar_last_error(h.h)
+        h.set_options(engine=engine)
+        ref, _ = oracle_expect(host, "float32", "sum", engine)
+        _, rows = upload(host, dev)
+        h.allreduce(rows)
+        h.check()
+        assert_bits_equal(rows, ref, "after timeout")
+
+
+def test_ring_straggler_keeps_results(rar, dev):
+    """An injected slow rank (pause before every slice) changes timing only."""
+    host = gen(4, 4 * 3000 + 1, "float32", ("normal", 1.0), 10)
+    run_case(rar, dev, host, "float32", "sum", "ring", fault_mode="delay", fault_rank=1,
+             fault_delay_ns=20_000, slice_elems=1024)
+
+
+@pytest.mark.parametrize("engine", ["fused", "ring", "ring_bidir"])
+def test_reduce_scatter_then_all_gather(rar, dev, engine):
+    """The two halves alone: after reduce-scatter rank r owns chunk (r + 1);
+    all-gather then completes the all-reduce."""
+    p, n = 8, 8 * 999 + 5
+    host = gen(p, n, "float32", ("normal", 1.0), 12)
+    full, _ = oracle_expect(host, "float32", "sum", engine)
+    _, rows = upload(host, dev)
+    with rar.Handle(0, engine=engine) as h:
+        h.reduce_scatter(rows)
+        h.check()
+        if engine == "ring":
+            rs = [w.to_storage_numpy(t).copy() for t in host]
+            oracle.simulate(rs, "float32", "sum", first_step=0, n_steps=p - 1)
+            assert_bits_equal(rows, rs, "ring reduce-scatter state")
+            assert h.send_counts(p) == [n - (e - s) for s, e in
+                                        [oracle.chunk_bounds(n, p)[(r + 1) % p] for r in range(p)]]
+        else:
+            segs = [(0, n, +1)] if engine == "fused" else [(0, n - n // 2, +1), (n - n // 2, n, -1)]
+            for lo, hi, d in segs:
+                for r in range(p):
+                    s, e = oracle.chunk_bounds(hi - lo, p)[(r + d) % p]
+                    got = w.to_storage_numpy(rows[r][lo + s:lo + e])
+                    assert np.array_equal(got, full[r][lo + s:lo + e])
+        h.all_gather(rows, )
+        h.check()
+    assert_bits_equal(rows, full, f"{engine} rs+ag")
+
+
+# ----------------------------------------------------------------- tree order
+
+def test_tree_order_bit_exact_and_bound(rar, dev):
+    for p in [2, 3, 4, 8, 16, 64]:
+        n = p * 300 + 7
+        host = gen(p, n, "float32", ("normal", 1.0), 100 + p)
+        run_case(rar, dev, host, "float32", "sum", "fused_tree")
+        _, rows = upload(host, dev)
+        with rar.Handle(0, engine="fused_tree") as h:
+            h.allreduce(rows)
+            h.check()
+        ref, mag = oracle.f64_sum([w.to_storage_numpy(t).copy() for t in host], "float32")
+        got = rows[0].cpu().double().numpy()
+        assert np.all(np.abs(got - ref) <= 4 * p * 2.0 ** -24 * mag)
+
+
+# ----------------------------------------------------------------- argument errors
+
+def test_argument_errors(rar, dev):
+    a = torch.zeros(4 * 100, device=dev)
+    with rar.Handle(0) as h:
+        # overlapping rank buffers
+        assert rar.rar_allreduce_ptrs(h.h, [a.data_ptr(), a.data_ptr() + 8], 100, "float32") == 1
+        # host pointer
+        c = torch.zeros(100)
+        assert rar.rar_allreduce_ptrs(h.h, [a.data_ptr(), c.data_ptr()], 100, "float32") == 1
+        # NULL rank pointer, p out of range
+        assert rar.rar_allreduce_ptrs(h.h, [a.data_ptr(), 0], 100, "float32") == 1
+        assert rar.rar_allreduce_ptrs(h.h, [], 100, "float32") == 1
+        # avg on int32 is not offered
+        i = torch.zeros(2, 10, dtype=torch.int32, device=dev)
+        with pytest.raises(rar.RarError) as e:
+            h.allreduce([i[0], i[1]], op="avg")
+        assert e.value.code == 2

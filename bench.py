@@ -1,0 +1,380 @@
+"""Benchmark: all-reduce algorithm bandwidth of the ring all-reduce engines.
+
+One step = one in-place all-reduce of the workload (p rank buffers of N
+elements) by the engine under test.  The headline workload is p = 8 virtual
+ranks, N = 2^30 bf16 elements per rank (16 GiB in total, far above the
+129 MB L2, so no flush is needed between steps), op = sum.
+
+    python bench.py [--steps K] [--warmup W] [--engine fused|ring|ring_bidir|all]
+    python bench.py --impl reference      # the CPU oracle on the host cores
+
+Metric: algBW = p * N * element bytes / time per step (GB/s), summed over
+GPUs when run under torchrun (independent replicas, weak scaling).  Also
+reported: each engine's fraction of the HBM roofline, with the roofline
+bytes 2 p N e (fused) and 5 (p - 1) N e (ring), against the measured copy
+bandwidth in MEASURED_PEAKS.json.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as w  # noqa: E402
+
+METRIC = "allreduce algBW GB/s (p·N·bytes/s) and % of GB300 HBM roofline, per engine"
+DTYPE_SHORT = {"bfloat16": "bf16", "float32": "f32", "int32": "i32", "float16": "f16"}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def roofline_bytes(engine: str, p: int, n: int, e: int) -> int:
+    """Minimum HBM bytes of one all-reduce: fused reads and writes every rank
+    once; the ring moves 3 elements per reduce-scatter hop and 2 per
+    all-gather hop over (p - 1) steps of n elements in total each."""
+    if engine in ("fused", "fused_tree"):
+        return 2 * p * n * e
+    return 5 * (p - 1) * n * e
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources, to tell whether stored ncu counters still
+    describe the kernels being timed."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ring_all_reduce_rar_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(engine: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    ent = d.get(workload, {}).get(engine)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) around the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed"], "samples": 0}
+        load = [s for s, pw in zip(sm, power) if pw > 200.0] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def time_engine(rar, engine, rows, op, steps, warmup, dist_ctx):
+    """Warm up, then time exactly `steps` all-reduces with CUDA events on the
+    stream the kernels are launched on."""
+    stream = torch.cuda.current_stream()
+    with rar.Handle(torch.cuda.current_device(), engine=engine, skip_pointer_check=True) as h:
+        for _ in range(warmup):
+            h.allreduce(rows, op=op, stream=stream)
+        h.check()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(steps):
+            h.allreduce(rows, op=op, stream=stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        dist_ctx.barrier()
+        rc = h.status()
+        if rc != 0:
+            raise RuntimeError(f"engine {engine}: device status {rc}: {rar.rar_last_error(h.h)}")
+        ms = start.elapsed_time(end)
+    return dist_ctx.max(ms)
+
+
+def time_e2e(rar, engine, host_rows, dev_rows, op, steps, warmup, dist_ctx):
+    """End to end through the public host-buffer call: every step copies the
+    rank buffers host -> device, all-reduces and copies all ranks back."""
+    stream = torch.cuda.current_stream()
+    with rar.Handle(torch.cuda.current_device(), engine=engine, skip_pointer_check=True) as h:
+        def step():
+            h.allreduce_host(host_rows, dev_rows, op=op, stream=stream)
+        for _ in range(warmup):
+            step()
+        h.check()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        dist_ctx.barrier()
+        ms = start.elapsed_time(end)
+    return dist_ctx.max(ms)
+
+
+class DistCtx:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+def cpu_baseline(cfg, op):
+    """The oracle as it stands, single-threaded on a host core, on a bounded
+    sample of the workload (same p and dtype, N = 2^25 per rank)."""
+    import numpy as np
+    import oracle
+    p, dtype = cfg["p"], cfg["dtype"]
+    n = 1 << 25 if cfg["n"] > (1 << 25) else cfg["n"]
+    _, rows = w.make_inputs(p, n, dtype, cfg["dist"], w.seed_of(cfg["index"]))
+    base = [w.to_storage_numpy(t).copy() for t in rows]
+    times = []
+    for _ in range(2):
+        bufs = [b.copy() for b in base]
+        t0 = time.perf_counter()
+        oracle.simulate(bufs, dtype, op)
+        times.append(time.perf_counter() - t0)
+    e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
+    t = min(times)
+    return {"value": round(p * n * e / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"schedule simulator, p={p}, N={n} {dtype} per rank (of N={cfg['n']}), op={op}, "
+                      f"best of {len(times)}, single thread"}
+
+
+def run_ours(args):
+    import ring_all_reduce_rar_gb300 as rar
+    rar.load_library()
+    ctx = DistCtx()
+    torch.cuda.set_device(ctx.local_rank)
+    dev = torch.device("cuda", ctx.local_rank)
+    cfg = w.WORKLOADS[args.workload]
+    p, n, dtype, op = cfg["p"], cfg["n"], cfg["dtype"], args.op or cfg["ops"][0]
+    e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
+    # each GPU holds its own replica of the workload (distinct seed per GPU)
+    seed = w.seed_of(cfg["index"]) + 1000 * ctx.rank
+    big, rows = w.make_inputs(p, n, dtype, cfg["dist"], seed, device=dev)
+    torch.cuda.synchronize()
+    engines = ["fused", "ring", "ring_bidir"] if args.engine == "all" else [args.engine]
+    peak, peak_kind = hbm_peak()
+    results = {}
+    with ClockSampler(ctx.local_rank) as clk:
+        for eng in engines:
+            ms = time_engine(rar, eng, rows, op, args.steps, args.warmup, ctx)
+            per_step = ms / args.steps
+            R = roofline_bytes(eng, p, n, e)
+            achieved = R / (per_step * 1e-3) / 1e9
+            results[eng] = {
+                "value": round(ctx.world * p * n * e / (per_step * 1e-3) / 1e9, 2),
+                "ms_per_step": round(per_step, 4),
+                "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                             "unit": "GB/s", "frac": round(achieved / peak, 4),
+                             "traffic": stored_traffic(eng, args.workload),
+                             "algorithmic_bytes": R, "peak_kind": f"of {peak_kind}"},
+            }
+    clocks = clk.summary()
+    head = engines[0]
+    e2e = None
+    if not args.no_e2e:
+        e2e_engine = head
+        host_rows = None
+        try:
+            host_big = torch.empty(big.shape, dtype=big.dtype, pin_memory=True)
+            host_big.copy_(big)
+            host_rows = [host_big[r, :n] for r in range(p)]
+        except RuntimeError as ex:
+            e2e = {"value": None, "unit": "GB/s", "unavailable": f"pinned host buffers: {ex}"[:200]}
+        if host_rows is not None:
+            ms = time_e2e(rar, e2e_engine, host_rows, rows, op, max(3, args.steps // 4), 1, ctx)
+            k = max(3, args.steps // 4)
+            e2e = {"value": round(ctx.world * p * n * e / (ms / k * 1e-3) / 1e9, 2), "unit": "GB/s",
+                   "h2d_bytes_per_step": p * n * e, "d2h_bytes_per_step": p * n * e,
+                   "engine": e2e_engine, "steps": k, "ms_per_step": round(ms / k, 3)}
+            del host_big, host_rows
+    cpu = None
+    if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, op)
+    if ctx.rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": results[head]["value"],
+            "unit": "GB/s",
+            "n_gpus": ctx.world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": results[head]["ms_per_step"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": DTYPE_SHORT[dtype],
+            "data": "synthetic (seeded splitmix64 inputs, N(0, 1e-2) in bf16)",
+            "config": {"workload": args.workload, "p": p, "n": n, "op": op, "engine": head,
+                       "l2": "inputs (16 GiB) larger than L2 (129 MB): no flush needed",
+                       "parallelism": "independent replica per GPU"},
+            "roofline": results[head]["roofline"],
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "engines": results,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The oracle (plain C simulator of the pages' schedule) on the host
+    cores, same metric and workload, one bounded sample per step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cfg = w.WORKLOADS[args.workload]
+    p, dtype, op = cfg["p"], cfg["dtype"], args.op or cfg["ops"][0]
+    n = min(cfg["n"], 1 << 22)
+    e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
+    _, rows = w.make_inputs(p, n, dtype, cfg["dist"], w.seed_of(cfg["index"]))
+    base = [w.to_storage_numpy(t).copy() for t in rows]
+    for _ in range(args.warmup):
+        oracle.simulate([b.copy() for b in base], dtype, op)
+    total = 0.0
+    for _ in range(args.steps):
+        bufs = [b.copy() for b in base]
+        t0 = time.perf_counter()
+        oracle.simulate(bufs, dtype, op)
+        total += time.perf_counter() - t0
+    per = total / args.steps
+    value = round(p * n * e / per / 1e9, 4)
+    sample = f"schedule simulator, p={p}, N={n} {dtype} per rank (of N={cfg['n']}), op={op}, single thread"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_SHORT[dtype],
+        "data": "synthetic", "config": {"workload": args.workload, "p": p, "n": cfg["n"], "op": op,
+                                        "engine": "oracle"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--engine", choices=["fused", "ring", "ring_bidir", "fused_tree", "all"], default="all")
+    ap.add_argument("--workload", choices=sorted(w.WORKLOADS), default="p8_n1073741824_bf16")
+    ap.add_argument("--op", choices=["sum", "avg", "max"], default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -139,6 +139,20 @@ int rar_reduce_scatter(rar_handle h, void *const *bufs, int p, size_t n, int dty
  * Same arguments and errors as rar_allreduce (op is not taken). */
 int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, void *stream);
 
+/* End-to-end form for host-resident data.  Enqueued on `stream`, in order:
+ * each host buffer is copied into the matching device buffer, the device
+ * buffers are all-reduced with the handle's engine (as rar_allreduce), and
+ * every rank's result is copied back into its host buffer.
+ *   host_bufs  host array of p host pointers, n elements each (pinned memory
+ *              keeps the copies asynchronous; pageable memory works, and the
+ *              copies then wait for the host)
+ *   dev_bufs   host array of p device pointers, n elements each: staging
+ *              buffers owned by the caller; they hold the result afterwards
+ * The library allocates nothing.  Errors: as rar_allreduce for dev_bufs, and
+ * RAR_EINVAL if host_bufs or one of its entries is NULL. */
+int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bufs, int p, size_t n, int dtype,
+                       int op, void *stream);
+
 /* Synchronise the stream of the last call and return its device-side
  * status: RAR_OK, RAR_ETIMEOUT (a wait ran out; rar_last_error names the
  * rank and step), or RAR_EABORTED.  A timed-out call leaves the buffers

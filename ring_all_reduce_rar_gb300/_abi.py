@@ -85,6 +85,7 @@ def load_library():
         for name in ("rar_allreduce", "rar_reduce_scatter"):
             getattr(lib, name).argtypes = [vp, ctypes.POINTER(vp), i32, sz, i32, i32, vp]
         lib.rar_all_gather.argtypes = [vp, ctypes.POINTER(vp), i32, sz, i32, vp]
+        lib.rar_allreduce_host.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, sz, i32, i32, vp]
         lib.rar_status.argtypes = [vp]
         lib.rar_send_counts.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i32]
         lib.rar_last_error.argtypes = [vp]
@@ -92,7 +93,7 @@ def load_library():
         lib.rar_destroy.argtypes = [vp]
         lib.rar_version.argtypes = []
         for name in ("rar_init", "rar_set_options", "rar_allreduce", "rar_reduce_scatter",
-                     "rar_all_gather", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
+                     "rar_all_gather", "rar_allreduce_host", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -168,6 +169,21 @@ def rar_all_gather(handle: int, tensors, stream=None) -> None:
     _check(handle, load_library().rar_all_gather(handle, arr, p, n, dt, _stream_ptr(stream, dev)))
 
 
+def rar_allreduce_host(handle: int, host_tensors, dev_tensors, op: str = "sum", stream=None) -> None:
+    """Host-resident buffers: copied in, all-reduced on the device staging
+    buffers, copied back (see rar_allreduce_host in rar.h)."""
+    import torch
+    arr, p, n, dt, dev = _marshal(dev_tensors)
+    if len(host_tensors) != p:
+        raise ValueError("need one host buffer per device buffer")
+    for t in host_tensors:
+        if t.device.type != "cpu" or not t.is_contiguous() or t.numel() != n or t.dtype != dev_tensors[0].dtype:
+            raise ValueError("host buffers must be contiguous CPU tensors matching the device buffers")
+    harr = (ctypes.c_void_p * p)(*[t.data_ptr() for t in host_tensors])
+    _check(handle, load_library().rar_allreduce_host(handle, harr, arr, p, n, dt, OP_CODES[op],
+                                                       _stream_ptr(stream, dev)))
+
+
 def rar_allreduce_ptrs(handle: int, ptrs, n: int, dtype: str, op: str = "sum", stream: int = 0) -> int:
     """Raw form: device pointers as ints; returns the status code (no raise)."""
     arr = (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
@@ -212,6 +228,9 @@ class Handle:
 
     def allreduce(self, tensors, op="sum", stream=None):
         rar_allreduce(self.h, tensors, op, stream)
+
+    def allreduce_host(self, host_tensors, dev_tensors, op="sum", stream=None):
+        rar_allreduce_host(self.h, host_tensors, dev_tensors, op, stream)
 
     def reduce_scatter(self, tensors, op="sum", stream=None):
         rar_reduce_scatter(self.h, tensors, op, stream)

@@ -323,6 +323,33 @@ int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, 
     return run(h, bufs, p, n, dtype, RAR_SUM, PHASE_AG, stream);
 }
 
+int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bufs, int p, size_t n, int dtype,
+                       int op, void *stream) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    h->err.clear();
+    if (!host_bufs) return fail(h, RAR_EINVAL, "host_bufs is NULL");
+    int rc = check_call(h, dev_bufs, p, n, dtype, op);
+    if (rc != RAR_OK) return rc;
+    for (int r = 0; r < p; r++)
+        if (!host_bufs[r]) return fail(h, RAR_EINVAL, "host buffer " + std::to_string(r) + " is NULL");
+    if (n == 0) return run(h, dev_bufs, p, n, dtype, op, PHASE_ALL, stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = n * (size_t)elem_bytes(dtype);
+    DeviceGuard dg(h->device);
+    if (dg.err != cudaSuccess) return cuda_fail(h, dg.err, "selecting the device");
+    for (int r = 0; r < p; r++) {
+        cudaError_t ce = cudaMemcpyAsync(dev_bufs[r], host_bufs[r], bytes, cudaMemcpyHostToDevice, s);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "copying a rank buffer to the device");
+    }
+    rc = run(h, dev_bufs, p, n, dtype, op, PHASE_ALL, stream);
+    if (rc != RAR_OK) return rc;
+    for (int r = 0; r < p; r++) {
+        cudaError_t ce = cudaMemcpyAsync(host_bufs[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, s);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "copying a result back to the host");
+    }
+    return RAR_OK;
+}
+
 int rar_status(rar_handle h) {
     if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
     if (!h->have_last) return RAR_OK;

@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for must in ("rar_init", "rar_allreduce", "rar_destroy", "rar_reduce_scatter", "rar_all_gather",
-                 "rar_status", "rar_send_counts", "rar_last_error", "rar_set_options", "rar_version"):
+                 "rar_status", "rar_send_counts", "rar_last_error", "rar_set_options", "rar_version",
+                 "rar_allreduce_host"):
         assert must in names
 
 

@@ -245,7 +245,9 @@ def run_ours(args):
     ctx = DistCtx()
     torch.cuda.set_device(ctx.local_rank)
     dev = torch.device("cuda", ctx.local_rank)
-    cfg = w.WORKLOADS[args.workload]
+    cfg = dict(w.WORKLOADS[args.workload])
+    if args.n:
+        cfg["n"] = args.n
     p, n, dtype, op = cfg["p"], cfg["n"], cfg["dtype"], args.op or cfg["ops"][0]
     e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
     # each GPU holds its own replica of the workload (distinct seed per GPU)
@@ -306,7 +308,8 @@ def run_ours(args):
             "dtype": DTYPE_SHORT[dtype],
             "data": "synthetic (seeded splitmix64 inputs, N(0, 1e-2) in bf16)",
             "config": {"workload": args.workload, "p": p, "n": n, "op": op, "engine": head,
-                       "l2": "inputs (16 GiB) larger than L2 (129 MB): no flush needed",
+                       "l2": f"inputs ({p * n * e / 2**30:.3g} GiB) vs L2 (129 MB): "
+                             + ("larger, no flush needed" if p * n * e > 4 * 129e6 else "NOT larger"),
                        "parallelism": "independent replica per GPU"},
             "roofline": results[head]["roofline"],
             "cpu_baseline": cpu,
@@ -366,6 +369,8 @@ def main():
     ap.add_argument("--engine", choices=["fused", "ring", "ring_bidir", "fused_tree", "all"], default="all")
     ap.add_argument("--workload", choices=sorted(w.WORKLOADS), default="p8_n1073741824_bf16")
     ap.add_argument("--op", choices=["sum", "avg", "max"], default=None)
+    ap.add_argument("--n", type=int, default=None,
+                    help="elements per rank instead of the workload's N (small cases for ncu captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -53,7 +53,8 @@
  *     in flight per handle: calls on one stream are ordered; calls on several
  *     streams with one handle must be ordered by the caller.
  *   - Trivial calls: p == 1 or n == 0 return RAR_OK and launch nothing (the
- *     torch ring in "An implementation" returns its tensor when p == 1).
+ *     torch ring in "An implementation" returns its tensor when p == 1);
+ *     with n == 0 the rank pointers may be NULL.
  */
 #ifndef RAR_H
 #define RAR_H

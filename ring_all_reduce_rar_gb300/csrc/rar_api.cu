@@ -94,9 +94,10 @@ int check_call(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op
     if (op == RAR_AVG && dtype == RAR_INT32) return fail(h, RAR_EUNSUPPORTED, "avg is not offered for int32");
     const size_t e = (size_t)elem_bytes(dtype);
     if (n > (size_t)(1ull << 62) / e) return fail(h, RAR_EINVAL, "n * element size overflows");
+    if (n == 0) return RAR_OK;  // nothing is accessed: NULL buffers are fine
     for (int r = 0; r < p; r++)
         if (!bufs[r]) return fail(h, RAR_EINVAL, "rank buffer " + std::to_string(r) + " is NULL");
-    if (n == 0 || p == 1) return RAR_OK;
+    if (p == 1) return RAR_OK;
     const size_t bytes = n * e;
     std::vector<std::pair<uintptr_t, int>> spans;
     spans.reserve((size_t)p);
@@ -330,9 +331,9 @@ int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bu
     if (!host_bufs) return fail(h, RAR_EINVAL, "host_bufs is NULL");
     int rc = check_call(h, dev_bufs, p, n, dtype, op);
     if (rc != RAR_OK) return rc;
+    if (n == 0) return run(h, dev_bufs, p, n, dtype, op, PHASE_ALL, stream);
     for (int r = 0; r < p; r++)
         if (!host_bufs[r]) return fail(h, RAR_EINVAL, "host buffer " + std::to_string(r) + " is NULL");
-    if (n == 0) return run(h, dev_bufs, p, n, dtype, op, PHASE_ALL, stream);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t bytes = n * (size_t)elem_bytes(dtype);
     DeviceGuard dg(h->device);

@@ -154,6 +154,29 @@ int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, 
 int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bufs, int p, size_t n, int dtype,
                        int op, void *stream);
 
+/* All-reduce for callers that may not allocate device memory: callers whose
+ * device memory belongs to another allocator (a framework's caching
+ * allocator, a pre-planned arena with a fixed budget), and callers that
+ * cannot pay for cudaMalloc/cudaFree at call time (both can block; cudaFree
+ * synchronises the device).  The source pages have no counterpart: this is
+ * the ring executor (RAR_ENGINE_RING, default tuning) without a handle,
+ * with its scratch -- progress words, receive counters, the status and the
+ * abort word -- in one fixed-size device array inside the library (about
+ * 16 KB, resident on every GPU that loads the library until exit).
+ * Arguments and results are as rar_allreduce's, on the current device.
+ * Limits: p <= 64 and p * channels <= 1024 CTAs; larger p returns
+ * RAR_EINVAL with a message from rar_last_error(NULL).
+ * The first call on a device, with that device current, sets the array up
+ * (takes its address and clears it once); make that first call before any
+ * stream capture.  Every call uses the same array: calls that overlap on
+ * the GPU (two streams, two threads) race and must be ordered by the caller.
+ * A ring wait that runs out (2 s) ends the kernel early and leaves the
+ * buffers partly reduced; without a handle this entry point cannot report
+ * it, so callers who need that status use rar_allreduce.
+ * Errors: as rar_allreduce, reported through the return value and
+ * rar_last_error(NULL). */
+int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dtype, int op, void *stream);
+
 /* Synchronise the stream of the last call and return its device-side
  * status: RAR_OK, RAR_ETIMEOUT (a wait ran out; rar_last_error names the
  * rank and step), or RAR_EABORTED.  A timed-out call leaves the buffers

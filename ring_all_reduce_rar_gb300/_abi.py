@@ -86,6 +86,7 @@ def load_library():
             getattr(lib, name).argtypes = [vp, ctypes.POINTER(vp), i32, sz, i32, i32, vp]
         lib.rar_all_gather.argtypes = [vp, ctypes.POINTER(vp), i32, sz, i32, vp]
         lib.rar_allreduce_host.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, sz, i32, i32, vp]
+        lib.rar_allreduce_noalloc.argtypes = [ctypes.POINTER(vp), i32, sz, i32, i32, vp]
         lib.rar_status.argtypes = [vp]
         lib.rar_send_counts.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i32]
         lib.rar_last_error.argtypes = [vp]
@@ -93,7 +94,7 @@ def load_library():
         lib.rar_destroy.argtypes = [vp]
         lib.rar_version.argtypes = []
         for name in ("rar_init", "rar_set_options", "rar_allreduce", "rar_reduce_scatter",
-                     "rar_all_gather", "rar_allreduce_host", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
+                     "rar_all_gather", "rar_allreduce_host", "rar_allreduce_noalloc", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -182,6 +183,13 @@ def rar_allreduce_host(handle: int, host_tensors, dev_tensors, op: str = "sum", 
     harr = (ctypes.c_void_p * p)(*[t.data_ptr() for t in host_tensors])
     _check(handle, load_library().rar_allreduce_host(handle, harr, arr, p, n, dt, OP_CODES[op],
                                                        _stream_ptr(stream, dev)))
+
+
+def rar_allreduce_noalloc(tensors, op: str = "sum", stream=None) -> None:
+    """Handle-free ring all-reduce that allocates no device memory (see
+    rar_allreduce_noalloc in rar.h); tensors on the current device."""
+    arr, p, n, dt, dev = _marshal(tensors)
+    _check(None, load_library().rar_allreduce_noalloc(arr, p, n, dt, OP_CODES[op], _stream_ptr(stream, dev)))
 
 
 def rar_allreduce_ptrs(handle: int, ptrs, n: int, dtype: str, op: str = "sum", stream: int = 0) -> int:

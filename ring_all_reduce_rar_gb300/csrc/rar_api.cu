@@ -247,6 +247,11 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
 
 }  // namespace
 
+namespace rar {
+// Message returned by rar_last_error(NULL) for entry points without a handle.
+void set_handleless_error(const std::string &msg) { g_init_error = msg; }
+}  // namespace rar
+
 extern "C" {
 
 int rar_version(void) { return RAR_VERSION; }

@@ -39,6 +39,7 @@ struct rar_ctx {
     cudaStream_t last_stream = nullptr;
     bool last_ring = false;
     unsigned last_epoch = 0;
+    unsigned last_status_epoch = 0;  // epoch of the last launch that can record a status (0: none)
     int last_p = 0;
     int last_channels = 0;
     int last_fwd_channels = 0;
@@ -137,6 +138,17 @@ int fill_ptrs(rar_ctx *h, RankPtrs &rp, void *const *bufs, int p, cudaStream_t s
     return RAR_OK;
 }
 
+// Next call epoch (never 0).  When the counter wraps, the progress words are
+// cleared once in stream order so that no stale word can satisfy a wait.
+int next_epoch(rar_ctx *h, cudaStream_t stream) {
+    if (++h->epoch == 0) {
+        cudaError_t ce = cudaMemsetAsync(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas, stream);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "resetting the progress words");
+        h->epoch = 1;
+    }
+    return RAR_OK;
+}
+
 bool all_aligned16(void *const *bufs, int p) {
     for (int r = 0; r < p; r++)
         if ((uintptr_t)bufs[r] % 16) return false;
@@ -152,6 +164,7 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     h->have_last = true;
     h->last_stream = stream;
     h->last_ring = false;
+    h->last_status_epoch = 0;
     h->last_p = p;
     if (n == 0 || p == 1) return RAR_OK;
 
@@ -169,7 +182,32 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         a.p = p;
         a.phase = phase;
         a.inv_p = inv_p;
+        a.status = h->status;
+        a.epoch = 0;
+        a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
         const bool tree = engine == RAR_ENGINE_FUSED_TREE && phase != PHASE_AG;
+        // data path: per-thread 128-bit loads (registers) or bulk-copy staging
+        const int tile = fused_bulk_tile_bytes(p);
+        const bool bulk_ok = engine == RAR_ENGINE_FUSED && phase == PHASE_ALL && vec16 && tile > 0 && p <= 128;
+        bool bulk = false;
+        if (h->opt.fused_path == 2) {
+            if (!bulk_ok)
+                return fail(h, RAR_EUNSUPPORTED,
+                            "the bulk-copy path needs engine fused, a full all-reduce, 16-byte aligned "
+                            "rank buffers and p <= 128");
+            bulk = true;
+        } else if (h->opt.fused_path == 0) {
+            bulk = bulk_ok && p > 16 && n * (size_t)elem_bytes(dtype) >= (size_t)tile * 64;
+        }
+        if (bulk) {
+            rc = next_epoch(h, stream);
+            if (rc != RAR_OK) return rc;
+            a.epoch = h->epoch;
+            cudaError_t ce = launch_fused_bulk(a, dtype, op, tile, 0, stream);
+            if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the bulk-copy fused kernel");
+            h->last_status_epoch = h->epoch;
+            return RAR_OK;
+        }
         const int threads = 256;  // the fused kernels are compiled for 256 threads
         cudaError_t ce = launch_fused(a, dtype, op, tree, vec16, threads, 0, stream);
         if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the fused kernel");
@@ -182,11 +220,11 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     if (threads > 512) return fail(h, RAR_EINVAL, "ring engines run at most 512 threads per CTA");
     int per_sm = 0;
     const int max_ctas = std::min(ring_max_coresident_ctas(dtype, op, vec16, threads, &per_sm), kMaxRingCtas);
+    // Defaults (from slice x channel x block sweeps on GB300): use every
+    // co-resident CTA, and give each channel one or a few large slices per
+    // step, since each slice hand-off costs a few microseconds.
     int G = h->opt.channels;
-    if (G == 0) {
-        // about two CTAs per SM in total, at least one (two when bidirectional) per rank
-        G = std::max(1, (2 * h->sm_count) / p);
-    }
+    if (G == 0) G = std::max(1, max_ctas / p);
     if (bidir && G < 2) G = 2;
     if ((long long)G * p > max_ctas) {
         if (h->opt.channels) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
@@ -196,23 +234,22 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     }
     const long long split = bidir ? (long long)n - (long long)n / 2 : (long long)n;  // chunk_bounds(n, 2)
     const int fwd_channels = bidir ? (G + 1) / 2 : G;
-    long long slice = h->opt.slice_elems ? h->opt.slice_elems : 16384;
-    slice = std::max<long long>(16, (slice + 15) / 16 * 16);
-    {
-        const long long maxchunk = (std::max(split, (long long)n - split) + p - 1) / p;
-        const int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
-        while ((maxchunk + slice - 1) / slice / min_g > kMaxSlicesPerChannelStep) slice *= 2;
+    const int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
+    const long long maxchunk = (std::max(split, (long long)n - split) + p - 1) / p;
+    long long slice = h->opt.slice_elems;
+    if (slice == 0) {
+        slice = (maxchunk + min_g - 1) / min_g;
+        slice = (slice + 1023) / 1024 * 1024;
+        slice = std::min<long long>(std::max<long long>(slice, 1024), 65536);
     }
+    slice = std::max<long long>(16, (slice + 15) / 16 * 16);
+    while ((maxchunk + slice - 1) / slice / min_g > kMaxSlicesPerChannelStep) slice *= 2;
 
     RingArgs a;
     rc = fill_ptrs(h, a.bufs, bufs, p, stream);
     if (rc != RAR_OK) return rc;
-    if (++h->epoch == 0) {
-        // epochs wrapped: clear the progress words once and restart at 1
-        cudaError_t ce = cudaMemsetAsync(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas, stream);
-        if (ce != cudaSuccess) return cuda_fail(h, ce, "resetting the progress words");
-        h->epoch = 1;
-    }
+    rc = next_epoch(h, stream);
+    if (rc != RAR_OK) return rc;
     a.n = (long long)n;
     a.p = p;
     a.channels = G;
@@ -240,6 +277,7 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     }
     h->last_ring = true;
     h->last_epoch = h->epoch;
+    h->last_status_epoch = h->epoch;
     h->last_channels = G;
     h->last_fwd_channels = fwd_channels;
     return RAR_OK;
@@ -362,16 +400,19 @@ int rar_status(rar_handle h) {
     DeviceGuard dg(h->device);
     cudaError_t ce = cudaStreamSynchronize(h->last_stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "synchronising the last call's stream");
-    if (!h->last_ring) return RAR_OK;
+    if (h->last_status_epoch == 0) return RAR_OK;
     RingStatus st{};
     ce = cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the status word");
-    if (st.epoch == h->last_epoch && st.code != 0) {
+    if (st.epoch == h->last_status_epoch && st.code != 0) {
         char buf[256];
-        std::snprintf(buf, sizeof(buf),
-                      "ring wait timed out: rank %d, step %d, slice %d, waiting on rank %d "
-                      "(progress word 0x%llx, wanted 0x%llx)",
-                      st.rank, st.step, st.slice, st.waited_on, st.flag_seen, st.flag_wanted);
+        if (st.rank >= 0)
+            std::snprintf(buf, sizeof(buf),
+                          "ring wait timed out: rank %d, step %d, slice %d, waiting on rank %d "
+                          "(progress word 0x%llx, wanted 0x%llx)",
+                          st.rank, st.step, st.slice, st.waited_on, st.flag_seen, st.flag_wanted);
+        else
+            std::snprintf(buf, sizeof(buf), "bulk-copy wait timed out on tile %d", st.slice);
         h->err = buf;
         return (int)st.code;
     }

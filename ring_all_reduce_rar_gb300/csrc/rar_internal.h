@@ -26,16 +26,7 @@ struct RankPtrs {
     void *const *table;  // device array of p pointers when p > kInlineP
 };
 
-// Fused engines: one launch covers [0, n) of every rank.
-struct FusedArgs {
-    RankPtrs bufs;
-    long long n;
-    int p;
-    int phase;     // Phase
-    float inv_p;   // binary32 nearest to 1/p
-};
-
-// Device-side status of a ring launch (written by the first CTA that gives up).
+// Device-side status of a launch (written by the first CTA that gives up).
 struct RingStatus {
     unsigned epoch;   // epoch of the call that failed (0: none yet)
     unsigned code;    // RAR_ETIMEOUT
@@ -45,6 +36,19 @@ struct RingStatus {
     int waited_on;    // neighbour rank it was waiting for
     unsigned long long flag_seen;
     unsigned long long flag_wanted;
+};
+
+// Fused engines: one launch covers [0, n) of every rank.
+struct FusedArgs {
+    RankPtrs bufs;
+    long long n;
+    int p;
+    int phase;     // Phase
+    float inv_p;   // binary32 nearest to 1/p
+    // bulk-copy path only: where a bounded wait that ran out is recorded
+    RingStatus *status;
+    unsigned epoch;
+    unsigned long long timeout_ns;
 };
 
 // Ring engines: persistent cooperative launch of p * channels CTAs.
@@ -79,6 +83,11 @@ cudaError_t launch_fused(const FusedArgs &a, int dtype, int op, bool tree, bool 
                          int threads, int grid_cap, cudaStream_t stream);
 cudaError_t launch_ring(const RingArgs &a, int dtype, int op, bool vec16, int threads,
                         cudaStream_t stream);
+// Bulk-copy (TMA) fused path: tile bytes per rank for p ranks (0: not
+// offered for this p), and the launcher (PHASE_ALL, 16-byte aligned ranks).
+int fused_bulk_tile_bytes(int p);
+cudaError_t launch_fused_bulk(const FusedArgs &a, int dtype, int op, int tile_bytes, int grid_cap,
+                              cudaStream_t stream);
 // Largest co-resident grid for the ring kernel of this dtype/op (per device).
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
 // Co-resident CTAs per SM for a fused kernel instance.

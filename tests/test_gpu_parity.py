@@ -15,7 +15,17 @@ import workloads as w
 
 pytestmark = pytest.mark.gpu
 
-RING_ENGINES = ["fused", "ring", "ring_bidir"]
+RING_ENGINES = ["fused", "fused_regs", "fused_bulk", "ring", "ring_bidir"]
+# "fused_regs" / "fused_bulk" force the fused engine's per-thread or
+# bulk-copy data path; "fused" lets the library choose
+ENGINE_OPTS = {"fused_regs": dict(engine="fused", fused_path="registers"),
+               "fused_bulk": dict(engine="fused", fused_path="bulk")}
+
+
+def handle_opts(engine, **opts):
+    o = dict(ENGINE_OPTS.get(engine, dict(engine=engine)))
+    o.update(opts)
+    return o
 
 
 @pytest.fixture(scope="module")
@@ -68,7 +78,9 @@ def assert_bits_equal(rows, ref, what=""):
 def run_case(rar, dev, host_rows, dtype, op, engine, offset=0, **opts):
     ref, sends = oracle_expect(host_rows, dtype, op, engine)
     _, rows = upload(host_rows, dev, offset)
-    with rar.Handle(0, engine=engine, **opts) as h:
+    if engine == "fused_bulk" and offset:
+        engine = "fused"  # the bulk path needs 16-byte aligned ranks
+    with rar.Handle(0, **handle_opts(engine, **opts)) as h:
         h.allreduce(rows, op=op)
         h.check()
         got_sends = h.send_counts(len(rows))
@@ -95,7 +107,7 @@ def test_page_trace_p4_n4(rar, dev, engine, dtype):
     vals = w.page_trace_inputs()
     host = [torch.tensor(v, dtype=torch.float32).to(w.TORCH_DTYPES[dtype]) for v in vals]
     _, rows = upload(host, dev)
-    with rar.Handle(0, engine=engine) as h:
+    with rar.Handle(0, **handle_opts(engine)) as h:
         h.allreduce(rows)
         h.check()
         sends = h.send_counts(4)
@@ -116,7 +128,7 @@ def test_semantics_example_p4_n1(rar, dev, engine):
     """"AllReduce 与 Ring 通信算法详解": [1, 2, 3, 4] -> 10 everywhere (N < p)."""
     host = [torch.tensor([float(r + 1)]) for r in range(4)]
     _, rows = upload(host, dev)
-    with rar.Handle(0, engine=engine) as h:
+    with rar.Handle(0, **handle_opts(engine)) as h:
         h.allreduce(rows)
         h.check()
         sends = h.send_counts(4)
@@ -187,7 +199,7 @@ def test_p64_n16777216_bf16_full_size_sampled(rar, dev, engine):
     cfg = w.WORKLOADS["p64_n16777216_bf16"]
     p, n, seed = cfg["p"], cfg["n"], w.seed_of(cfg["index"])
     big, rows = w.make_inputs(p, n, cfg["dtype"], cfg["dist"], seed, device=dev)
-    with rar.Handle(0, engine=engine) as h:
+    with rar.Handle(0, **handle_opts(engine)) as h:
         h.allreduce(rows)
         h.check()
     check_sampled(rows, p, n, cfg["dtype"], cfg["dist"], seed, "sum", engine)
@@ -204,7 +216,7 @@ def test_p8_n2pow30_bf16_full_size_sampled(rar, dev, engine):
     cpu = w.sample_inputs(seed, p, idx, cfg["dist"], cfg["dtype"])
     for r in range(p):
         assert torch.equal(rows[r][idx.to(dev)].cpu(), cpu[r])
-    with rar.Handle(0, engine=engine) as h:
+    with rar.Handle(0, **handle_opts(engine)) as h:
         h.allreduce(rows)
         h.check()
     check_sampled(rows, p, n, cfg["dtype"], cfg["dist"], seed, "sum", engine)
@@ -226,7 +238,7 @@ def test_p16_sweep(rar, dev, engine, pair):
             run_case(rar, dev, host, dtype, op, engine)
         else:
             big, rows = w.make_inputs(p, n, dtype, dist, seed, device=dev)
-            with rar.Handle(0, engine=engine) as h:
+            with rar.Handle(0, **handle_opts(engine)) as h:
                 h.allreduce(rows, op=op)
                 h.check()
             check_sampled(rows, p, n, dtype, dist, seed, op, engine, m=50_000)
@@ -276,7 +288,7 @@ def test_large_p_uses_pointer_table(rar, dev, engine):
 def test_trivial_calls(rar, dev, engine):
     one = [torch.arange(10, dtype=torch.float32, device=dev)]
     empty = [torch.zeros(0, device=dev) for _ in range(4)]
-    with rar.Handle(0, engine=engine) as h:
+    with rar.Handle(0, **handle_opts(engine)) as h:
         h.allreduce(one)
         h.allreduce(empty)
         h.check()
@@ -360,7 +372,7 @@ def test_reduce_scatter_then_all_gather(rar, dev, engine):
     host = gen(p, n, "float32", ("normal", 1.0), 12)
     full, _ = oracle_expect(host, "float32", "sum", engine)
     _, rows = upload(host, dev)
-    with rar.Handle(0, engine=engine) as h:
+    with rar.Handle(0, **handle_opts(engine)) as h:
         h.reduce_scatter(rows)
         h.check()
         if engine == "ring":

@@ -102,10 +102,15 @@ typedef struct {
     int fault_mode;                /* rar_fault_mode, ring engines only (tests) */
     int fault_rank;                /* rank the fault applies to */
     unsigned fault_delay_ns;       /* RAR_FAULT_DELAY: pause before each slice */
-    int fused_path;                /* RAR_ENGINE_FUSED data path: 0 auto, 1 per-thread
-                                      128-bit loads and stores, 2 bulk-copy (TMA)
-                                      staging in shared memory (all-reduce, 16-byte
-                                      aligned ranks, p <= 128); same results */
+    int fused_path;                /* RAR_ENGINE_FUSED data path, same results on both:
+                                      0 auto; 1 per-thread 128-bit loads of all p
+                                      ranks and streaming stores; 2 rank-sequential
+                                      streaming: bulk copies (TMA) of one rank tile
+                                      at a time in hop order into shared memory,
+                                      running values in registers, bulk stores of
+                                      the result (full all-reduce, 16-byte aligned
+                                      ranks; slice_elems = tile elements per rank,
+                                      channels = pipeline stages, 0 = auto) */
 } rar_options;
 
 /* Create a handle on `device`; allocates the ring engines' flags, counters

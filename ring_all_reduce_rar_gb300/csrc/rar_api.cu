@@ -83,6 +83,7 @@ int check_options(rar_ctx *h, const rar_options &o) {
         return fail(h, RAR_EINVAL, "block_threads must be a multiple of 32, at most 1024");
     if (o.fault_mode < RAR_FAULT_NONE || o.fault_mode > RAR_FAULT_DELAY)
         return fail(h, RAR_EINVAL, "unknown fault_mode");
+    if (o.fused_path < 0 || o.fused_path > 2) return fail(h, RAR_EINVAL, "unknown fused_path");
     return RAR_OK;
 }
 
@@ -186,25 +187,31 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         a.epoch = 0;
         a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
         const bool tree = engine == RAR_ENGINE_FUSED_TREE && phase != PHASE_AG;
-        // data path: per-thread 128-bit loads (registers) or bulk-copy staging
-        const int tile = fused_bulk_tile_bytes(p);
-        const bool bulk_ok = engine == RAR_ENGINE_FUSED && phase == PHASE_ALL && vec16 && tile > 0 && p <= 128;
-        bool bulk = false;
-        if (h->opt.fused_path == 2) {
-            if (!bulk_ok)
-                return fail(h, RAR_EUNSUPPORTED,
-                            "the bulk-copy path needs engine fused, a full all-reduce, 16-byte aligned "
-                            "rank buffers and p <= 128");
-            bulk = true;
-        } else if (h->opt.fused_path == 0) {
-            bulk = bulk_ok && p > 16 && n * (size_t)elem_bytes(dtype) >= (size_t)tile * 64;
-        }
-        if (bulk) {
+        // data path: per-thread 128-bit loads ("registers") or the
+        // rank-sequential bulk-copy streaming path.  Auto (measured on GB300):
+        // registers for p <= 16 below 80 MB per rank, streaming otherwise.
+        const size_t bytes = n * (size_t)elem_bytes(dtype);
+        const bool stream_ok = engine == RAR_ENGINE_FUSED && phase == PHASE_ALL && vec16;
+        int path = h->opt.fused_path;
+        if (path == 2 && !stream_ok)
+            return fail(h, RAR_EUNSUPPORTED,
+                        "the streaming path needs engine fused, a full all-reduce and 16-byte aligned rank buffers");
+        if (path == 0) path = (stream_ok && (p > 16 || bytes >= (size_t)80 << 20)) ? 2 : 1;
+        if (path == 2) {
             rc = next_epoch(h, stream);
             if (rc != RAR_OK) return rc;
             a.epoch = h->epoch;
-            cudaError_t ce = launch_fused_bulk(a, dtype, op, tile, 0, stream);
-            if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the bulk-copy fused kernel");
+            // tile per rank (slice_elems, else 32 KB, halved while there are
+            // fewer than four tiles per SM); stages (channels, else 3)
+            size_t tb = h->opt.slice_elems ? (size_t)h->opt.slice_elems * (size_t)elem_bytes(dtype) : 32768;
+            tb = std::min<size_t>(std::max<size_t>(tb / 512 * 512, 512), 32768);
+            if (!h->opt.slice_elems)
+                while (tb > 512 && bytes / tb < (size_t)(4 * h->sm_count)) tb /= 2;
+            const int stages = h->opt.channels ? h->opt.channels : 3;
+            if (stages < 2 || stages > 8 || (size_t)(stages + 2) * tb > 227 * 1024)
+                return fail(h, RAR_EINVAL, "streaming path: stages (channels) must be in [2, 8] and fit in 227 KB");
+            cudaError_t ce = launch_fused_stream(a, dtype, op, (int)tb, stages, stream);
+            if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the streaming fused kernel");
             h->last_status_epoch = h->epoch;
             return RAR_OK;
         }

@@ -45,7 +45,7 @@ struct FusedArgs {
     int p;
     int phase;     // Phase
     float inv_p;   // binary32 nearest to 1/p
-    // bulk-copy path only: where a bounded wait that ran out is recorded
+    // streaming path only: where a bounded wait that ran out is recorded
     RingStatus *status;
     unsigned epoch;
     unsigned long long timeout_ns;
@@ -83,11 +83,11 @@ cudaError_t launch_fused(const FusedArgs &a, int dtype, int op, bool tree, bool 
                          int threads, int grid_cap, cudaStream_t stream);
 cudaError_t launch_ring(const RingArgs &a, int dtype, int op, bool vec16, int threads,
                         cudaStream_t stream);
-// Bulk-copy (TMA) fused path: tile bytes per rank for p ranks (0: not
-// offered for this p), and the launcher (PHASE_ALL, 16-byte aligned ranks).
-int fused_bulk_tile_bytes(int p);
-cudaError_t launch_fused_bulk(const FusedArgs &a, int dtype, int op, int tile_bytes, int grid_cap,
-                              cudaStream_t stream);
+// Rank-sequential streaming fused path (PHASE_ALL, 16-byte aligned ranks);
+// tile_bytes per rank in [512, 32768], a multiple of 512; n_stages in [2, 8];
+// (n_stages + 2) tiles must fit in 227 KB of shared memory.
+cudaError_t launch_fused_stream(const FusedArgs &a, int dtype, int op, int tile_bytes, int n_stages,
+                                cudaStream_t stream);
 // Largest co-resident grid for the ring kernel of this dtype/op (per device).
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
 // Co-resident CTAs per SM for a fused kernel instance.

@@ -15,11 +15,11 @@ import workloads as w
 
 pytestmark = pytest.mark.gpu
 
-RING_ENGINES = ["fused", "fused_regs", "fused_bulk", "ring", "ring_bidir"]
-# "fused_regs" / "fused_bulk" force the fused engine's per-thread or
-# bulk-copy data path; "fused" lets the library choose
+RING_ENGINES = ["fused", "fused_regs", "fused_stream", "ring", "ring_bidir"]
+# "fused_regs" / "fused_stream" force the fused engine's per-thread or
+# streaming (bulk-copy) data path; "fused" lets the library choose
 ENGINE_OPTS = {"fused_regs": dict(engine="fused", fused_path="registers"),
-               "fused_bulk": dict(engine="fused", fused_path="bulk")}
+               "fused_stream": dict(engine="fused", fused_path="stream")}
 
 
 def handle_opts(engine, **opts):
@@ -78,8 +78,8 @@ def assert_bits_equal(rows, ref, what=""):
 def run_case(rar, dev, host_rows, dtype, op, engine, offset=0, **opts):
     ref, sends = oracle_expect(host_rows, dtype, op, engine)
     _, rows = upload(host_rows, dev, offset)
-    if engine == "fused_bulk" and offset:
-        engine = "fused"  # the bulk path needs 16-byte aligned ranks
+    if engine == "fused_stream" and offset:
+        engine = "fused"  # the streaming path needs 16-byte aligned ranks
     with rar.Handle(0, **handle_opts(engine, **opts)) as h:
         h.allreduce(rows, op=op)
         h.check()

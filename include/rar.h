@@ -149,17 +149,20 @@ int rar_reduce_scatter(rar_handle h, void *const *bufs, int p, size_t n, int dty
  * Same arguments and errors as rar_allreduce (op is not taken). */
 int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, void *stream);
 
-/* End-to-end form for host-resident data.  Enqueued on `stream`, in order:
- * each host buffer is copied into the matching device buffer, the device
- * buffers are all-reduced with the handle's engine (as rar_allreduce), and
- * every rank's result is copied back into its host buffer.
- *   host_bufs  host array of p host pointers, n elements each (pinned memory
- *              keeps the copies asynchronous; pageable memory works, and the
- *              copies then wait for the host)
- *   dev_bufs   host array of p device pointers, n elements each: staging
- *              buffers owned by the caller; they hold the result afterwards
- * The library allocates nothing.  Errors: as rar_allreduce for dev_bufs, and
- * RAR_EINVAL if host_bufs or one of its entries is NULL. */
+/* All-reduce of host-resident rank buffers, with the handle's engine.
+ *   host_bufs  host array of p host pointers, n elements each; the result
+ *              replaces the inputs
+ *   dev_bufs   host array of p device pointers (n elements each, owned by
+ *              the caller), or NULL; used only for pageable host memory
+ * If every host buffer is page-locked and mapped for the handle's device
+ * (cudaHostAlloc, or torch's pin_memory), the kernel reads the inputs and
+ * writes the results over the host link itself, in one pass, and dev_bufs is
+ * not touched.  Otherwise the buffers are staged, in stream order: each host
+ * buffer is copied into dev_bufs[r], those are all-reduced (as
+ * rar_allreduce), and the results are copied back (these copies wait for the
+ * host when the memory is pageable).  The library allocates nothing.
+ * Errors: as rar_allreduce; RAR_EINVAL if host_bufs or an entry is NULL, or
+ * the memory is pageable and dev_bufs is NULL. */
 int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bufs, int p, size_t n, int dtype,
                        int op, void *stream);
 

@@ -174,19 +174,30 @@ def rar_all_gather(handle: int, tensors, stream=None) -> None:
     _check(handle, load_library().rar_all_gather(handle, arr, p, n, dt, _stream_ptr(stream, dev)))
 
 
-def rar_allreduce_host(handle: int, host_tensors, dev_tensors, op: str = "sum", stream=None) -> None:
-    """Host-resident buffers: copied in, all-reduced on the device staging
-    buffers, copied back (see rar_allreduce_host in rar.h)."""
+def rar_allreduce_host(handle: int, host_tensors, dev_tensors=None, op: str = "sum", stream=None) -> None:
+    """All-reduce host-resident buffers (see rar_allreduce_host in rar.h):
+    pinned host tensors are reduced in place by the GPU over the host link;
+    pageable ones are staged through dev_tensors."""
     import torch
-    arr, p, n, dt, dev = _marshal(dev_tensors)
-    if len(host_tensors) != p:
-        raise ValueError("need one host buffer per device buffer")
+    names = {torch.int32: "int32", torch.float32: "float32", torch.bfloat16: "bfloat16", torch.float16: "float16"}
+    p = len(host_tensors)
+    if p < 1:
+        raise ValueError("need at least one rank buffer")
+    t0 = host_tensors[0]
+    if t0.dtype not in names:
+        raise ValueError(f"unsupported dtype {t0.dtype}")
     for t in host_tensors:
-        if t.device.type != "cpu" or not t.is_contiguous() or t.numel() != n or t.dtype != dev_tensors[0].dtype:
-            raise ValueError("host buffers must be contiguous CPU tensors matching the device buffers")
+        if t.device.type != "cpu" or not t.is_contiguous() or t.numel() != t0.numel() or t.dtype != t0.dtype:
+            raise ValueError("host buffers must be contiguous CPU tensors of one dtype and length")
     harr = (ctypes.c_void_p * p)(*[t.data_ptr() for t in host_tensors])
-    _check(handle, load_library().rar_allreduce_host(handle, harr, arr, p, n, dt, OP_CODES[op],
-                                                       _stream_ptr(stream, dev)))
+    if dev_tensors is not None:
+        darr, dp, dn, dt, dev = _marshal(dev_tensors)
+        if dp != p or dn != t0.numel() or dev_tensors[0].dtype != t0.dtype:
+            raise ValueError("device staging buffers must match the host buffers")
+    else:
+        darr, dev = None, torch.device("cuda", torch.cuda.current_device())
+    _check(handle, load_library().rar_allreduce_host(handle, harr, darr, p, t0.numel(), DTYPE_CODES[names[t0.dtype]],
+                                                       OP_CODES[op], _stream_ptr(stream, dev)))
 
 
 def rar_allreduce_noalloc(tensors, op: str = "sum", stream=None) -> None:
@@ -241,7 +252,7 @@ class Handle:
     def allreduce(self, tensors, op="sum", stream=None):
         rar_allreduce(self.h, tensors, op, stream)
 
-    def allreduce_host(self, host_tensors, dev_tensors, op="sum", stream=None):
+    def allreduce_host(self, host_tensors, dev_tensors=None, op="sum", stream=None):
         rar_allreduce_host(self.h, host_tensors, dev_tensors, op, stream)
 
     def reduce_scatter(self, tensors, op="sum", stream=None):

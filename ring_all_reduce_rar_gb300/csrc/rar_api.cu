@@ -88,7 +88,8 @@ int check_options(rar_ctx *h, const rar_options &o) {
 }
 
 // Argument checks shared by every collective (include/rar.h, rar_allreduce).
-int check_call(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op) {
+// host_mapped: the pointers are device aliases of page-locked host memory.
+int check_call(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, bool host_mapped = false) {
     if (!bufs) return fail(h, RAR_EINVAL, "bufs is NULL");
     if (p < 1 || p > RAR_MAX_P) return fail(h, RAR_EINVAL, "p must be in [1, RAR_MAX_P]");
     if (dtype < RAR_INT32 || dtype > RAR_FLOAT16) return fail(h, RAR_EINVAL, "unknown dtype");
@@ -109,7 +110,7 @@ int check_call(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op
         if (spans[k].first < spans[k - 1].first + bytes)
             return fail(h, RAR_EINVAL, "rank buffers " + std::to_string(spans[k - 1].second) + " and " +
                                            std::to_string(spans[k].second) + " overlap");
-    if (!h->opt.skip_pointer_check) {
+    if (!h->opt.skip_pointer_check && !host_mapped) {
         for (int r = 0; r < p; r++) {
             cudaPointerAttributes at{};
             cudaError_t ce = cudaPointerGetAttributes(&at, bufs[r]);
@@ -156,10 +157,11 @@ bool all_aligned16(void *const *bufs, int p) {
     return true;
 }
 
-int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int phase, void *stream_v) {
+int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int phase, void *stream_v,
+        bool host_mapped = false) {
     if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
     h->err.clear();
-    int rc = check_call(h, bufs, p, n, dtype, op);
+    int rc = check_call(h, bufs, p, n, dtype, op, host_mapped);
     if (rc != RAR_OK) return rc;
     cudaStream_t stream = (cudaStream_t)stream_v;
     h->have_last = true;
@@ -379,15 +381,35 @@ int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bu
     if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
     h->err.clear();
     if (!host_bufs) return fail(h, RAR_EINVAL, "host_bufs is NULL");
-    int rc = check_call(h, dev_bufs, p, n, dtype, op);
-    if (rc != RAR_OK) return rc;
-    if (n == 0) return run(h, dev_bufs, p, n, dtype, op, PHASE_ALL, stream);
+    if (p < 1 || p > RAR_MAX_P) return fail(h, RAR_EINVAL, "p must be in [1, RAR_MAX_P]");
+    if (n == 0) return run(h, host_bufs, p, n, dtype, op, PHASE_ALL, stream, true);
     for (int r = 0; r < p; r++)
         if (!host_bufs[r]) return fail(h, RAR_EINVAL, "host buffer " + std::to_string(r) + " is NULL");
-    cudaStream_t s = (cudaStream_t)stream;
-    const size_t bytes = n * (size_t)elem_bytes(dtype);
     DeviceGuard dg(h->device);
     if (dg.err != cudaSuccess) return cuda_fail(h, dg.err, "selecting the device");
+    // Zero copy: page-locked host memory mapped for this device is read and
+    // written by the kernel itself over the host link, in one pass.
+    std::vector<void *> mapped((size_t)p, nullptr);
+    bool zero_copy = true;
+    for (int r = 0; r < p && zero_copy; r++) {
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, host_bufs[r]) != cudaSuccess) {
+            cudaGetLastError();
+            zero_copy = false;
+        } else if (at.type == cudaMemoryTypeHost && at.devicePointer) {
+            mapped[(size_t)r] = at.devicePointer;
+        } else {
+            zero_copy = false;
+        }
+    }
+    if (zero_copy) return run(h, mapped.data(), p, n, dtype, op, PHASE_ALL, stream, true);
+
+    // Staged: pageable host memory goes through the caller's device buffers.
+    if (!dev_bufs) return fail(h, RAR_EINVAL, "host buffers are not page-locked and dev_bufs is NULL");
+    int rc = check_call(h, dev_bufs, p, n, dtype, op);
+    if (rc != RAR_OK) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = n * (size_t)elem_bytes(dtype);
     for (int r = 0; r < p; r++) {
         cudaError_t ce = cudaMemcpyAsync(dev_bufs[r], host_bufs[r], bytes, cudaMemcpyHostToDevice, s);
         if (ce != cudaSuccess) return cuda_fail(h, ce, "copying a rank buffer to the device");

@@ -409,6 +409,34 @@ def test_tree_order_bit_exact_and_bound(rar, dev):
         assert np.all(np.abs(got - ref) <= 4 * p * 2.0 ** -24 * mag)
 
 
+# ----------------------------------------------------------------- host buffers
+
+@pytest.mark.parametrize("engine", ["fused", "fused_stream", "ring"])
+def test_allreduce_host_pinned_and_pageable(rar, dev, engine):
+    """rar_allreduce_host: pinned host buffers are reduced in place by the GPU
+    (zero copy); pageable ones are staged through device buffers.  Both equal
+    the oracle bit for bit."""
+    p, n = 8, 8 * 5000 + 5
+    host = gen(p, n, "bfloat16", ("normal", 1e-2), 77)
+    ref, _ = oracle_expect(host, "bfloat16", "sum", "ring")
+    pinned = [t.clone().pin_memory() for t in host]
+    with rar.Handle(0, **handle_opts(engine)) as h:
+        h.allreduce_host(pinned)
+        h.check()
+        torch.cuda.synchronize()
+        assert_bits_equal(pinned, ref, f"{engine} pinned")
+        pageable = [t.clone() for t in host]
+        _, staging = upload(host, dev)
+        h.allreduce_host(pageable, staging)
+        h.check()
+        torch.cuda.synchronize()
+        assert_bits_equal(pageable, ref, f"{engine} pageable")
+        assert_bits_equal(staging, ref, f"{engine} staging")
+        with pytest.raises(rar.RarError) as e:
+            h.allreduce_host([t.clone() for t in host])
+        assert e.value.code == 1
+
+
 # ----------------------------------------------------------------- argument errors
 
 def test_argument_errors(rar, dev):

@@ -71,7 +71,15 @@ extern "C" {
 typedef struct rar_ctx *rar_handle;
 
 typedef enum { RAR_INT32 = 0, RAR_FLOAT32 = 1, RAR_BFLOAT16 = 2, RAR_FLOAT16 = 3 } rar_dtype;
-typedef enum { RAR_SUM = 0, RAR_MAX = 1, RAR_AVG = 2 } rar_op;
+typedef enum {
+    RAR_SUM = 0,
+    RAR_MAX = 1,
+    RAR_AVG = 2,        /* ring-order sum, then x 1/p at the chunk's owner */
+    RAR_AVG_PREDIV = 3  /* every rank's element x 1/p (rounded to the dtype) as it
+                           enters the ring, then the ring-order sum: a 16-bit sum over
+                           many ranks cannot overflow ("Ring All-Reduce, in depth",
+                           "Failure modes": pre-divide) */
+} rar_op;
 typedef enum {
     RAR_ENGINE_FUSED = 0,
     RAR_ENGINE_RING = 1,
@@ -127,7 +135,7 @@ int rar_set_options(rar_handle h, const rar_options *opt);
  * Errors: RAR_EINVAL (null handle/array/pointer, p < 1 or p > RAR_MAX_P,
  * unknown dtype or op, n * element size overflows, overlapping buffers,
  * pointers not device memory of the handle's device), RAR_EUNSUPPORTED
- * (avg on int32; ring engine grid cannot be co-resident), RAR_ECUDA. */
+ * (avg or avg_prediv on int32; ring engine grid cannot be co-resident), RAR_ECUDA. */
 int rar_allreduce(rar_handle h, void *const *bufs, int p, size_t n, int dtype, int op,
                   void *stream);
 

@@ -34,7 +34,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "librar_oracle.so")
 
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2, "float16": 3}
-OPS = {"sum": 0, "max": 1, "avg": 2}
+OPS = {"sum": 0, "max": 1, "avg": 2, "avg_prediv": 3}
 MODES = {"ring": 0, "bidir": 1, "tree": 2}
 _STORAGE = {"int32": np.int32, "float32": np.float32, "bfloat16": np.uint16, "float16": np.uint16}
 

@@ -202,9 +202,15 @@ static void scale_by_inv_p(int dtype, void *elem, int p)
 static int valid_kind(int dtype, int op)
 {
     if (orc_elem_size(dtype) == 0) return 0;
-    if (op != ORC_SUM && op != ORC_MAX && op != ORC_AVG) return 0;
-    if (op == ORC_AVG && dtype == ORC_I32) return 0;
+    if (op != ORC_SUM && op != ORC_MAX && op != ORC_AVG && op != ORC_AVG_PREDIV) return 0;
+    if ((op == ORC_AVG || op == ORC_AVG_PREDIV) && dtype == ORC_I32) return 0;
     return 1;
+}
+
+/* The op a hop applies: both averages add. */
+static int hop_of(int op)
+{
+    return (op == ORC_AVG || op == ORC_AVG_PREDIV) ? ORC_SUM : op;
 }
 
 static int mod_p(int64_t v, int p)
@@ -246,7 +252,13 @@ int orc_ring_simulate(void *const *bufs, int p, int64_t n, int dtype, int op,
     unsigned char *msg = (unsigned char *)malloc((size_t)p * (size_t)(maxlen > 0 ? maxlen : 1) * (size_t)es);
     if (!msg) { free(starts); free(msg_chunk); return -1; }
 
-    int hop_op = (op == ORC_AVG) ? ORC_SUM : op;
+    int hop_op = hop_of(op);
+    /* pre-divide: each rank scales its own contribution before the ring */
+    if (op == ORC_AVG_PREDIV && first_step == 0) {
+        for (int r = 0; r < p; r++)
+            for (int64_t i = 0; i < n; i++)
+                scale_by_inv_p(dtype, (unsigned char *)bufs[r] + (size_t)i * (size_t)es, p);
+    }
     for (int step = first_step; step < first_step + n_steps; step++) {
         int reduce = step < p - 1;
         int s = reduce ? step : step - (p - 1);
@@ -369,15 +381,19 @@ int orc_fold_sampled(const void *vals, const int64_t *idx, int64_t m, int p,
     } else {
         orc_chunk_bounds(n, p, fwd);
     }
-    int hop_op = (op == ORC_AVG) ? ORC_SUM : op;
+    int hop_op = hop_of(op);
     int rc = 0;
     for (int64_t j = 0; j < m; j++) {
         int64_t i = idx[j];
         if (i < 0 || i >= n) { rc = -1; break; }
         unsigned char acc[4];
+        /* rank r's contribution at this index (pre-divided if asked) */
+        for (int r = 0; r < p; r++) {
+            memcpy(tmp + (size_t)r * (size_t)es, v + ((size_t)r * (size_t)m + (size_t)j) * (size_t)es, (size_t)es);
+            if (op == ORC_AVG_PREDIV)
+                scale_by_inv_p(dtype, tmp + (size_t)r * (size_t)es, p);
+        }
         if (mode == 2) {
-            for (int r = 0; r < p; r++)
-                memcpy(tmp + (size_t)r * (size_t)es, v + ((size_t)r * (size_t)m + (size_t)j) * (size_t)es, (size_t)es);
             tree_levels(dtype, hop_op, tmp, p);
             memcpy(acc, tmp, (size_t)es);
         } else {
@@ -389,10 +405,10 @@ int orc_fold_sampled(const void *vals, const int64_t *idx, int64_t m, int p,
                 c = chunk_of(fwd, p, i);
                 dir = +1;
             }
-            memcpy(acc, v + ((size_t)c * (size_t)m + (size_t)j) * (size_t)es, (size_t)es);
+            memcpy(acc, tmp + (size_t)c * (size_t)es, (size_t)es);
             for (int k = 1; k < p; k++) {
                 int r = mod_p((int64_t)c + (int64_t)dir * k, p);
-                orc_combine(dtype, hop_op, acc, v + ((size_t)r * (size_t)m + (size_t)j) * (size_t)es, acc);
+                orc_combine(dtype, hop_op, acc, tmp + (size_t)r * (size_t)es, acc);
             }
         }
         if (op == ORC_AVG)
@@ -412,10 +428,13 @@ int orc_tree_fold(void *const *bufs, int p, int64_t n, int dtype, int op)
     int es = orc_elem_size(dtype);
     unsigned char *tmp = (unsigned char *)malloc((size_t)p * (size_t)es);
     if (!tmp) return -1;
-    int hop_op = (op == ORC_AVG) ? ORC_SUM : op;
+    int hop_op = hop_of(op);
     for (int64_t i = 0; i < n; i++) {
-        for (int r = 0; r < p; r++)
+        for (int r = 0; r < p; r++) {
             memcpy(tmp + (size_t)r * (size_t)es, (unsigned char *)bufs[r] + (size_t)i * (size_t)es, (size_t)es);
+            if (op == ORC_AVG_PREDIV)
+                scale_by_inv_p(dtype, tmp + (size_t)r * (size_t)es, p);
+        }
         tree_levels(dtype, hop_op, tmp, p);
         if (op == ORC_AVG)
             scale_by_inv_p(dtype, tmp, p);

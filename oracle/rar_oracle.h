@@ -27,7 +27,11 @@
  *
  * Element types and ops (codes are the oracle's own):
  *   dtype: ORC_I32 = 0, ORC_F32 = 1, ORC_BF16 = 2, ORC_F16 = 3
- *   op:    ORC_SUM = 0, ORC_MAX = 1, ORC_AVG = 2 (float types only)
+ *   op:    ORC_SUM = 0, ORC_MAX = 1, ORC_AVG = 2 (float types only),
+ *          ORC_AVG_PREDIV = 3 (float types only): every rank's contribution
+ *          is multiplied by 1/p, rounded to the dtype, before the ring-order
+ *          sum ("Ring All-Reduce, in depth", "Failure modes": pre-divide so
+ *          that a sum over many ranks cannot overflow)
  * Buffers are arrays of the element type in host memory; bf16 and f16 are
  * passed as their raw 16-bit patterns.
  */
@@ -41,7 +45,7 @@ extern "C" {
 #endif
 
 enum { ORC_I32 = 0, ORC_F32 = 1, ORC_BF16 = 2, ORC_F16 = 3 };
-enum { ORC_SUM = 0, ORC_MAX = 1, ORC_AVG = 2 };
+enum { ORC_SUM = 0, ORC_MAX = 1, ORC_AVG = 2, ORC_AVG_PREDIV = 3 };
 
 /* Ring direction for the simulator and the per-element fold. */
 enum { ORC_FORWARD = 0,   /* rank r sends to r + 1 (the pages' ring)            */
@@ -72,7 +76,9 @@ void orc_combine(int dtype, int op, const void *acc, const void *own, void *out)
  *             p-1 .. 2p-3 are all-gather; (0, 2p-2) is the whole all-reduce,
  *             (0, p-1) the reduce-scatter alone, (p-1, p-1) the all-gather
  *             alone.  For op ORC_AVG the owner scales its chunk by 1/p right
- *             after the last reduce-scatter step (step p-2), if that step ran.
+ *             after the last reduce-scatter step (step p-2), if that step ran;
+ *             for ORC_AVG_PREDIV every rank scales its own buffer by 1/p
+ *             before step 0, if step 0 runs.
  *   sends     nullable; p counters, incremented by the elements each rank sent
  * Returns 0, or -1 on bad arguments.  p == 1 and n == 0 are no-ops. */
 int orc_ring_simulate(void *const *bufs, int p, int64_t n, int dtype, int op,

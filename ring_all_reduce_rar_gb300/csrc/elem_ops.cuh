@@ -95,6 +95,14 @@ __device__ __forceinline__ uint32_t scale_word(uint32_t w, float inv_p) {
     }
 }
 
+// A rank's contribution as it enters the fold: unchanged, or (pre-divided
+// average) times 1/p rounded to the dtype.
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t contrib_word(uint32_t w, float inv_p) {
+    if constexpr (OP == OP_AVG_PREDIV) return scale_word<DT>(w, inv_p);
+    else return w;
+}
+
 template <int DT, int OP>
 __device__ __forceinline__ uint4 hop_vec(uint4 acc, uint4 own) {
     acc.x = hop_word<DT, OP>(acc.x, own.x);
@@ -112,6 +120,16 @@ __device__ __forceinline__ uint4 scale_vec(uint4 v, float inv_p) {
     v.w = scale_word<DT>(v.w, inv_p);
     return v;
 }
+
+template <int DT, int OP>
+__device__ __forceinline__ uint4 contrib_vec(uint4 v, float inv_p) {
+    if constexpr (OP == OP_AVG_PREDIV) return scale_vec<DT>(v, inv_p);
+    else return v;
+}
+
+// The op a hop applies: both averages add.
+template <int OP>
+struct HopOf { static constexpr int value = (OP == OP_AVG || OP == OP_AVG_PREDIV) ? OP_SUM : OP; };
 
 // Single elements (16-bit types use the low half of the word).
 template <int DT>

@@ -43,10 +43,11 @@ __device__ __forceinline__ void fused_fold_vectors(const FusedArgs &a, int p, in
         }
         return;
     }
+    constexpr int hop = HopOf<OP>::value;
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, p, c));
 #pragma unroll
-        for (int u = 0; u < U; u++) acc[u] = __ldcs(src + v0 + u * stride);
+        for (int u = 0; u < U; u++) acc[u] = contrib_vec<DT, OP>(__ldcs(src + v0 + u * stride), a.inv_p);
     }
     if constexpr (P > 0) {
         uint4 own[P > 1 ? P - 1 : 1][U];
@@ -61,7 +62,7 @@ __device__ __forceinline__ void fused_fold_vectors(const FusedArgs &a, int p, in
 #pragma unroll
         for (int k = 1; k < P; k++)
 #pragma unroll
-            for (int u = 0; u < U; u++) acc[u] = hop_vec<DT, OP>(acc[u], own[k - 1][u]);
+            for (int u = 0; u < U; u++) acc[u] = hop_vec<DT, hop>(acc[u], contrib_vec<DT, OP>(own[k - 1][u], a.inv_p));
     } else {
         constexpr int G = 8;
         for (int k0 = 1; k0 < p; k0 += G) {
@@ -81,7 +82,8 @@ __device__ __forceinline__ void fused_fold_vectors(const FusedArgs &a, int p, in
             for (int j = 0; j < G; j++)
                 if (k0 + j < p)
 #pragma unroll
-                    for (int u = 0; u < U; u++) acc[u] = hop_vec<DT, OP>(acc[u], own[j][u]);
+                    for (int u = 0; u < U; u++)
+                        acc[u] = hop_vec<DT, hop>(acc[u], contrib_vec<DT, OP>(own[j][u], a.inv_p));
         }
     }
     if constexpr (OP == OP_AVG) {
@@ -112,11 +114,12 @@ __device__ __forceinline__ void fused_fold_element(const FusedArgs &a, int p, in
             if (r != owner) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
         return;
     }
-    acc = load_elem<DT>(rank_ptr(a.bufs, p, c), i);
+    constexpr int hop = HopOf<OP>::value;
+    acc = contrib_word<DT, OP>(load_elem<DT>(rank_ptr(a.bufs, p, c), i), a.inv_p);
     for (int k = 1; k < p; k++) {
         int r = c + k;
         r -= (r >= p) ? p : 0;
-        acc = hop_word<DT, OP>(acc, load_elem<DT>(rank_ptr(a.bufs, p, r), i));
+        acc = hop_word<DT, hop>(acc, contrib_word<DT, OP>(load_elem<DT>(rank_ptr(a.bufs, p, r), i), a.inv_p));
     }
     if constexpr (OP == OP_AVG) acc = scale_word<DT>(acc, a.inv_p);
     if (a.phase == PHASE_RS) {
@@ -181,12 +184,13 @@ __device__ __forceinline__ uint4 tree_fold_vector(const FusedArgs &a, int p, lon
     uint4 st[kMaxDepth];
     int sz[kMaxDepth];
     int sp = 0;
+    constexpr int hop = HopOf<OP>::value;
     auto push = [&](int r, int pp) {
-        st[sp] = __ldcs(reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, pp, r)) + v);
+        st[sp] = contrib_vec<DT, OP>(__ldcs(reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, pp, r)) + v), a.inv_p);
         sz[sp] = 1;
         sp++;
         while (sp >= 2 && sz[sp - 1] == sz[sp - 2]) {
-            st[sp - 2] = hop_vec<DT, OP>(st[sp - 2], st[sp - 1]);
+            st[sp - 2] = hop_vec<DT, hop>(st[sp - 2], st[sp - 1]);
             sz[sp - 2] *= 2;
             sp--;
         }
@@ -198,7 +202,7 @@ __device__ __forceinline__ uint4 tree_fold_vector(const FusedArgs &a, int p, lon
         for (int r = 0; r < p; r++) push(r, p);
     }
     while (sp > 1) {
-        st[sp - 2] = hop_vec<DT, OP>(st[sp - 2], st[sp - 1]);
+        st[sp - 2] = hop_vec<DT, hop>(st[sp - 2], st[sp - 1]);
         sp--;
     }
     return st[0];
@@ -210,18 +214,19 @@ __device__ __forceinline__ uint32_t tree_fold_element(const FusedArgs &a, int p,
     uint32_t st[kMaxDepth];
     int sz[kMaxDepth];
     int sp = 0;
+    constexpr int hop = HopOf<OP>::value;
     for (int r = 0; r < p; r++) {
-        st[sp] = load_elem<DT>(rank_ptr(a.bufs, p, r), i);
+        st[sp] = contrib_word<DT, OP>(load_elem<DT>(rank_ptr(a.bufs, p, r), i), a.inv_p);
         sz[sp] = 1;
         sp++;
         while (sp >= 2 && sz[sp - 1] == sz[sp - 2]) {
-            st[sp - 2] = hop_word<DT, OP>(st[sp - 2], st[sp - 1]);
+            st[sp - 2] = hop_word<DT, hop>(st[sp - 2], st[sp - 1]);
             sz[sp - 2] *= 2;
             sp--;
         }
     }
     while (sp > 1) {
-        st[sp - 2] = hop_word<DT, OP>(st[sp - 2], st[sp - 1]);
+        st[sp - 2] = hop_word<DT, hop>(st[sp - 2], st[sp - 1]);
         sp--;
     }
     return st[0];

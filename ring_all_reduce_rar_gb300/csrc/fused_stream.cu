@@ -107,11 +107,12 @@ __device__ __noinline__ void stream_straddling_vector(const FusedArgs &a, int p,
     for (int l = 0; l < VE; l++) {
         const long long i = i0 + l;
         const int c = chunk_of(i, base, extra);
-        uint32_t acc = load_elem<DT>(rank_ptr(a.bufs, p, c), i);
+        uint32_t acc = contrib_word<DT, OP>(load_elem<DT>(rank_ptr(a.bufs, p, c), i), a.inv_p);
         for (int k = 1; k < p; k++) {
             int r = c + k;
             r -= (r >= p) ? p : 0;
-            acc = hop_word<DT, OP == OP_AVG ? OP_SUM : OP>(acc, load_elem<DT>(rank_ptr(a.bufs, p, r), i));
+            acc = hop_word<DT, HopOf<OP>::value>(acc, contrib_word<DT, OP>(load_elem<DT>(rank_ptr(a.bufs, p, r), i),
+                                                                          a.inv_p));
         }
         if constexpr (OP == OP_AVG) acc = scale_word<DT>(acc, a.inv_p);
         if constexpr (EB == 4) reinterpret_cast<uint32_t *>(out)[l] = acc;
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     __shared__ int s_fail;
     constexpr int EB = ElemInfo<DT>::bytes;
     constexpr int VE = 16 / EB;
-    constexpr int hop_op = OP == OP_AVG ? OP_SUM : OP;
+    constexpr int hop_op = HopOf<OP>::value;
     const int p = a.p;
     const int TB = tile_bytes;
     const int NS = n_stages;
@@ -247,7 +248,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     if (v >= nvec || seg[u] < 0) continue;
                     const int kk = j - seg[u];
                     if (kk >= 0 && kk < p) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(st + (size_t)v * 16);
+                        const uint4 x = contrib_vec<DT, OP>(*reinterpret_cast<const uint4 *>(st + (size_t)v * 16),
+                                                            a.inv_p);
                         acc[u] = kk == 0 ? x : hop_vec<DT, hop_op>(acc[u], x);
                     }
                 }
@@ -365,16 +367,19 @@ cudaError_t launch_fused_stream(const FusedArgs &a, int dtype, int op, int tile_
         if (op == OP_SUM) return launch_stream_t<DT_F32, OP_SUM>(a, tile_bytes, n_stages, stream);
         if (op == OP_MAX) return launch_stream_t<DT_F32, OP_MAX>(a, tile_bytes, n_stages, stream);
         if (op == OP_AVG) return launch_stream_t<DT_F32, OP_AVG>(a, tile_bytes, n_stages, stream);
+        if (op == OP_AVG_PREDIV) return launch_stream_t<DT_F32, OP_AVG_PREDIV>(a, tile_bytes, n_stages, stream);
         break;
     case DT_BF16:
         if (op == OP_SUM) return launch_stream_t<DT_BF16, OP_SUM>(a, tile_bytes, n_stages, stream);
         if (op == OP_MAX) return launch_stream_t<DT_BF16, OP_MAX>(a, tile_bytes, n_stages, stream);
         if (op == OP_AVG) return launch_stream_t<DT_BF16, OP_AVG>(a, tile_bytes, n_stages, stream);
+        if (op == OP_AVG_PREDIV) return launch_stream_t<DT_BF16, OP_AVG_PREDIV>(a, tile_bytes, n_stages, stream);
         break;
     case DT_F16:
         if (op == OP_SUM) return launch_stream_t<DT_F16, OP_SUM>(a, tile_bytes, n_stages, stream);
         if (op == OP_MAX) return launch_stream_t<DT_F16, OP_MAX>(a, tile_bytes, n_stages, stream);
         if (op == OP_AVG) return launch_stream_t<DT_F16, OP_AVG>(a, tile_bytes, n_stages, stream);
+        if (op == OP_AVG_PREDIV) return launch_stream_t<DT_F16, OP_AVG_PREDIV>(a, tile_bytes, n_stages, stream);
         break;
     }
     return cudaErrorInvalidValue;

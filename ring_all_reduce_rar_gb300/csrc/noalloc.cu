@@ -76,8 +76,8 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     if (!bufs) return reject(RAR_EINVAL, "bufs is NULL");
     if (p < 1 || p > kInlineP) return reject(RAR_EINVAL, "p must be in [1, 64] (limit of this entry point)");
     if (dtype < RAR_INT32 || dtype > RAR_FLOAT16) return reject(RAR_EINVAL, "unknown dtype");
-    if (op < RAR_SUM || op > RAR_AVG) return reject(RAR_EINVAL, "unknown op");
-    if (op == RAR_AVG && dtype == RAR_INT32) return reject(RAR_EUNSUPPORTED, "avg is not offered for int32");
+    if (op < RAR_SUM || op > RAR_AVG_PREDIV) return reject(RAR_EINVAL, "unknown op");
+    if ((op == RAR_AVG || op == RAR_AVG_PREDIV) && dtype == RAR_INT32) return reject(RAR_EUNSUPPORTED, "avg is not offered for int32");
     const size_t e = (size_t)elem_bytes(dtype);
     if (n > (size_t)(1ull << 62) / e) return reject(RAR_EINVAL, "n * element size overflows");
     if (n == 0) return RAR_OK;

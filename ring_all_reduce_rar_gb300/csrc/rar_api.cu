@@ -93,8 +93,8 @@ int check_call(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op
     if (!bufs) return fail(h, RAR_EINVAL, "bufs is NULL");
     if (p < 1 || p > RAR_MAX_P) return fail(h, RAR_EINVAL, "p must be in [1, RAR_MAX_P]");
     if (dtype < RAR_INT32 || dtype > RAR_FLOAT16) return fail(h, RAR_EINVAL, "unknown dtype");
-    if (op < RAR_SUM || op > RAR_AVG) return fail(h, RAR_EINVAL, "unknown op");
-    if (op == RAR_AVG && dtype == RAR_INT32) return fail(h, RAR_EUNSUPPORTED, "avg is not offered for int32");
+    if (op < RAR_SUM || op > RAR_AVG_PREDIV) return fail(h, RAR_EINVAL, "unknown op");
+    if ((op == RAR_AVG || op == RAR_AVG_PREDIV) && dtype == RAR_INT32) return fail(h, RAR_EUNSUPPORTED, "avg is not offered for int32");
     const size_t e = (size_t)elem_bytes(dtype);
     if (n > (size_t)(1ull << 62) / e) return fail(h, RAR_EINVAL, "n * element size overflows");
     if (n == 0) return RAR_OK;  // nothing is accessed: NULL buffers are fine

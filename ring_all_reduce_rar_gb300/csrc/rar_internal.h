@@ -14,7 +14,7 @@ namespace rar {
 constexpr int kInlineP = 64;
 
 enum Dtype { DT_I32 = RAR_INT32, DT_F32 = RAR_FLOAT32, DT_BF16 = RAR_BFLOAT16, DT_F16 = RAR_FLOAT16 };
-enum Op { OP_SUM = RAR_SUM, OP_MAX = RAR_MAX, OP_AVG = RAR_AVG };
+enum Op { OP_SUM = RAR_SUM, OP_MAX = RAR_MAX, OP_AVG = RAR_AVG, OP_AVG_PREDIV = RAR_AVG_PREDIV };
 
 // Which part of the schedule a launch runs.
 enum Phase { PHASE_ALL = 0, PHASE_RS = 1, PHASE_AG = 2 };

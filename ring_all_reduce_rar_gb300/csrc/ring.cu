@@ -114,17 +114,25 @@ __device__ void ring_delay(unsigned ns) {
 // owner's avg scaling if `scale`.
 template <int DT, int OP, bool VEC>
 __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
-                                           bool scale, float inv_p) {
-    constexpr int hop_op = OP == OP_AVG ? OP_SUM : OP;
+                                           bool scale, bool first_hop, float inv_p) {
+    constexpr int hop_op = HopOf<OP>::value;
+    constexpr bool prediv = OP == OP_AVG_PREDIV;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
     const int T = blockDim.x;
     long long vlo = (lo + VE - 1) / VE, vhi = hi / VE;
     if (!VEC || vlo >= vhi) vlo = vhi = lo / VE;  // all of it on the element path
     const long long elo = VEC ? vlo * VE : lo;      // [lo, elo) and [ehi, hi) per element
     const long long ehi = VEC ? vhi * VE : lo;
+    // pre-divided average: the receiver's own element enters scaled, and so
+    // does the incoming one at reduce-scatter step 0 (the sender's original)
     auto one = [&](long long i) {
         uint32_t x = load_elem<DT>(src, i);
-        if (reduce) x = hop_word<DT, hop_op>(x, load_elem<DT>(dst, i));
+        if (reduce) {
+            if (prediv && first_hop) x = scale_word<DT>(x, inv_p);
+            uint32_t own = load_elem<DT>(dst, i);
+            if (prediv) own = scale_word<DT>(own, inv_p);
+            x = hop_word<DT, hop_op>(x, own);
+        }
         if (OP == OP_AVG && scale) x = scale_word<DT>(x, inv_p);
         store_elem<DT>(dst, i, x);
     };
@@ -155,7 +163,10 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
             const long long vv = v + (long long)u * T;
             if (vv < vhi) {
                 uint4 x = in[u];
-                if (reduce) x = hop_vec<DT, hop_op>(x, own[u]);
+                if (reduce) {
+                    if (prediv && first_hop) x = scale_vec<DT>(x, inv_p);
+                    x = hop_vec<DT, hop_op>(x, prediv ? scale_vec<DT>(own[u], inv_p) : own[u]);
+                }
                 if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
                 d4[vv] = x;
             }
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
                 {
                     const long long lo = cs + sl * a.slice;
                     const long long hi = lo + a.slice < ce ? lo + a.slice : ce;
-                    ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale, a.inv_p);
+                    ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale, rs && s == 0, a.inv_p);
                     received += (unsigned long long)(hi - lo);
                 }
                 __syncthreads();
@@ -248,16 +259,19 @@ cudaError_t launch_ring(const RingArgs &a, int dtype, int op, bool vec16, int th
         if (op == OP_SUM) return launch_ring_op<DT_F32, OP_SUM>(a, vec16, threads, stream);
         if (op == OP_MAX) return launch_ring_op<DT_F32, OP_MAX>(a, vec16, threads, stream);
         if (op == OP_AVG) return launch_ring_op<DT_F32, OP_AVG>(a, vec16, threads, stream);
+        if (op == OP_AVG_PREDIV) return launch_ring_op<DT_F32, OP_AVG_PREDIV>(a, vec16, threads, stream);
         break;
     case DT_BF16:
         if (op == OP_SUM) return launch_ring_op<DT_BF16, OP_SUM>(a, vec16, threads, stream);
         if (op == OP_MAX) return launch_ring_op<DT_BF16, OP_MAX>(a, vec16, threads, stream);
         if (op == OP_AVG) return launch_ring_op<DT_BF16, OP_AVG>(a, vec16, threads, stream);
+        if (op == OP_AVG_PREDIV) return launch_ring_op<DT_BF16, OP_AVG_PREDIV>(a, vec16, threads, stream);
         break;
     case DT_F16:
         if (op == OP_SUM) return launch_ring_op<DT_F16, OP_SUM>(a, vec16, threads, stream);
         if (op == OP_MAX) return launch_ring_op<DT_F16, OP_MAX>(a, vec16, threads, stream);
         if (op == OP_AVG) return launch_ring_op<DT_F16, OP_AVG>(a, vec16, threads, stream);
+        if (op == OP_AVG_PREDIV) return launch_ring_op<DT_F16, OP_AVG_PREDIV>(a, vec16, threads, stream);
         break;
     }
     return cudaErrorInvalidValue;
@@ -283,17 +297,20 @@ int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *ou
     case DT_F32:
         per_sm = op == OP_SUM ? ring_occ<DT_F32, OP_SUM>(vec16, threads)
                  : op == OP_MAX ? ring_occ<DT_F32, OP_MAX>(vec16, threads)
-                                : ring_occ<DT_F32, OP_AVG>(vec16, threads);
+                 : op == OP_AVG ? ring_occ<DT_F32, OP_AVG>(vec16, threads)
+                                : ring_occ<DT_F32, OP_AVG_PREDIV>(vec16, threads);
         break;
     case DT_BF16:
         per_sm = op == OP_SUM ? ring_occ<DT_BF16, OP_SUM>(vec16, threads)
                  : op == OP_MAX ? ring_occ<DT_BF16, OP_MAX>(vec16, threads)
-                                : ring_occ<DT_BF16, OP_AVG>(vec16, threads);
+                 : op == OP_AVG ? ring_occ<DT_BF16, OP_AVG>(vec16, threads)
+                                : ring_occ<DT_BF16, OP_AVG_PREDIV>(vec16, threads);
         break;
     default:
         per_sm = op == OP_SUM ? ring_occ<DT_F16, OP_SUM>(vec16, threads)
                  : op == OP_MAX ? ring_occ<DT_F16, OP_MAX>(vec16, threads)
-                                : ring_occ<DT_F16, OP_AVG>(vec16, threads);
+                 : op == OP_AVG ? ring_occ<DT_F16, OP_AVG>(vec16, threads)
+                                : ring_occ<DT_F16, OP_AVG_PREDIV>(vec16, threads);
         break;
     }
     int dev = 0, sms = 0;

@@ -260,7 +260,8 @@ def test_odd_p_ragged_n_and_small_n(rar, dev, engine):
 @pytest.mark.parametrize("engine", RING_ENGINES)
 @pytest.mark.parametrize("dtype,op", [("int32", "max"), ("bfloat16", "max"), ("bfloat16", "avg"),
                                       ("float16", "sum"), ("float16", "avg"), ("float16", "max"),
-                                      ("int32", "sum"), ("float32", "max")])
+                                      ("int32", "sum"), ("float32", "max"), ("float32", "avg_prediv"),
+                                      ("bfloat16", "avg_prediv"), ("float16", "avg_prediv")])
 def test_dtype_op_matrix(rar, dev, engine, dtype, op):
     dist = ("uniform_int", -(1 << 20), 21) if dtype == "int32" else ("normal", 1.0)
     for p, n in [(4, 4099), (8, 8 * 777 + 5), (6, 1001)]:
@@ -308,6 +309,22 @@ def test_bf16_subnormals_and_ties(rar, dev):
     host = [torch.from_numpy(np.roll(vals, r).astype(np.int16)).view(torch.bfloat16) for r in range(5)]
     for engine in RING_ENGINES:
         run_case(rar, dev, host, "bfloat16", "sum", engine)
+
+
+@pytest.mark.parametrize("engine", RING_ENGINES + ["fused_tree"])
+def test_prediv_fp16_no_overflow(rar, dev, engine):
+    """16 ranks of fp16 4096: the post-divided average overflows to inf (the
+    sum 65536 exceeds 65504), the pre-divided one is exactly 4096."""
+    p, n = 16, 16 * 64 + 3
+    host = [torch.full((n,), 4096.0, dtype=torch.float16) for _ in range(p)]
+    for op, expect in [("avg", float("inf")), ("avg_prediv", 4096.0)]:
+        _, rows = upload(host, dev)
+        with rar.Handle(0, **handle_opts(engine)) as h:
+            h.allreduce(rows, op=op)
+            h.check()
+        torch.cuda.synchronize()
+        for t in rows:
+            assert torch.all(t.float() == expect), (engine, op)
 
 
 # ----------------------------------------------------------------- ring engine specifics

@@ -294,9 +294,42 @@ def test_avg_any_p_exact_rational(dtype):
             assert got == e, (p, i)
 
 
+def test_prediv_avoids_fp16_overflow():
+    """"Ring All-Reduce, in depth", "Failure modes": summing fp16 from many
+    ranks can overflow; pre-dividing avoids it.  16 ranks of 4096: the sum
+    65536 exceeds the largest fp16 value (65504) and rounds to inf, so the
+    post-divided average is inf; pre-divided, each contribution is 256
+    (exact) and the sum is exactly 4096, the true mean."""
+    p, n = 16, 10
+    h4096 = oracle.f32_to_f16(4096.0)
+    post = [np.full(n, h4096, dtype=np.uint16) for _ in range(p)]
+    oracle.simulate(post, "float16", "avg")
+    assert all(oracle.f16_to_f32(int(v)) == float("inf") for v in post[0])
+    pre = [np.full(n, h4096, dtype=np.uint16) for _ in range(p)]
+    oracle.simulate(pre, "float16", "avg_prediv")
+    for b in pre:
+        assert all(oracle.f16_to_f32(int(v)) == 4096.0 for v in b)
+
+
+def test_prediv_exact_mean_when_division_is_exact():
+    """For p a power of two and inputs that are multiples of p, every
+    pre-divided contribution and every partial sum is exact: the result is
+    the exact mean."""
+    for p in [2, 4, 8, 16]:
+        n = 50
+        ints = [rng.integers(-40, 41, size=n) for _ in range(p)]
+        bufs = [(v * p).astype(np.float32) for v in ints]
+        oracle.simulate(bufs, "float32", "avg_prediv")
+        mean = np.sum(np.stack(ints), axis=0).astype(np.float32)
+        for b in bufs:
+            np.testing.assert_array_equal(b, mean)
+
+
 def test_avg_rejected_for_int32():
     with pytest.raises(ValueError):
         oracle.simulate(_rand_i32(4, 8), "int32", "avg")
+    with pytest.raises(ValueError):
+        oracle.simulate(_rand_i32(4, 8), "int32", "avg_prediv")
 
 
 # ------------------------------------------------------------- float sums
@@ -461,7 +494,8 @@ def test_fp32_add_is_ieee():
 CASES = [
     ("int32", "sum"), ("int32", "max"), ("float32", "sum"), ("float32", "max"),
     ("float32", "avg"), ("bfloat16", "sum"), ("bfloat16", "max"), ("bfloat16", "avg"),
-    ("float16", "sum"), ("float16", "avg"),
+    ("float16", "sum"), ("float16", "avg"), ("float32", "avg_prediv"), ("bfloat16", "avg_prediv"),
+    ("float16", "avg_prediv"),
 ]
 
 

@@ -119,6 +119,14 @@ typedef struct {
                                       the result (full all-reduce, 16-byte aligned
                                       ranks; slice_elems = tile elements per rank,
                                       channels = pipeline stages, 0 = auto) */
+    int hier_group;                /* 0 (or 1 or p): the flat ring.  g with 1 < g < p, g | p:
+                                      the hierarchical 2D schedule over p / g nodes of g
+                                      consecutive ranks ("Ring All-Reduce, in depth",
+                                      "Hierarchy"): reduce-scatter inside each node,
+                                      all-reduce of each 1/g shard across the nodes, all-gather
+                                      inside each node.  Full all-reduce only; RAR_ENGINE_RING
+                                      runs it as three ring launches, RAR_ENGINE_FUSED folds in
+                                      its order on the per-thread path */
 } rar_options;
 
 /* Create a handle on `device`; allocates the ring engines' flags, counters

@@ -87,6 +87,9 @@ def _load():
                                                 ctypes.POINTER(i64)]
         lib.orc_fold_sampled.argtypes = [vp, ctypes.POINTER(i64), i64, i32, i64, i32, i32, i32, vp]
         lib.orc_tree_fold.argtypes = [ctypes.POINTER(vp), i32, i64, i32, i32]
+        lib.orc_hier_simulate.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i32, i32,
+                                          ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.orc_hier_fold_sampled.argtypes = [vp, ctypes.POINTER(i64), i64, i32, i32, i64, i32, i32, vp]
         lib.orc_f64_sum.argtypes = [ctypes.POINTER(vp), i32, i64, i32,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
         _lib = lib
@@ -174,6 +177,34 @@ def fold_sampled(vals: np.ndarray, idx: np.ndarray, n: int, dtype: str, op: str 
                               m, p, n, DTYPES[dtype], OPS[op], MODES[mode], out.ctypes.data)
     if rc != 0:
         raise ValueError("orc_fold_sampled rejected its arguments")
+    return out
+
+
+def hier_simulate(bufs, g: int, dtype: str, op: str = "sum"):
+    """Hierarchical 2D all-reduce with nodes of g ranks, in place; returns
+    (intra-node sends, cross-node sends) per rank."""
+    lib = _load()
+    n = _check_bufs(bufs, dtype)
+    p = len(bufs)
+    si = (ctypes.c_int64 * max(1, p))()
+    sx = (ctypes.c_int64 * max(1, p))()
+    rc = lib.orc_hier_simulate(_ptr_array(bufs), p, g, n, DTYPES[dtype], OPS[op], si, sx)
+    if rc != 0:
+        raise ValueError("orc_hier_simulate rejected its arguments")
+    return np.array(si[:p], dtype=np.int64), np.array(sx[:p], dtype=np.int64)
+
+
+def hier_fold_sampled(vals: np.ndarray, idx: np.ndarray, n: int, g: int, dtype: str, op: str = "sum"):
+    """Hierarchical all-reduced value at sampled indices (vals: (p, m))."""
+    lib = _load()
+    vals = np.ascontiguousarray(vals)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    p, m = vals.shape
+    out = np.empty(m, dtype=vals.dtype)
+    rc = lib.orc_hier_fold_sampled(vals.ctypes.data, idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), m, p, g,
+                                   n, DTYPES[dtype], OPS[op], out.ctypes.data)
+    if rc != 0:
+        raise ValueError("orc_hier_fold_sampled rejected its arguments")
     return out
 
 

@@ -462,3 +462,113 @@ int orc_f64_sum(const void *const *bufs, int p, int64_t n, int dtype,
     }
     return 0;
 }
+
+/* ------------------------------------------------------- hierarchical ring */
+
+/* "Ring All-Reduce, in depth", "Hierarchy" / "Worked example": the three
+ * phases below, each a ring of the schedule above on a subset of the ranks
+ * (declared in rar_oracle.h). */
+int orc_hier_simulate(void *const *bufs, int p, int g, int64_t n, int dtype,
+                      int op, int64_t *sends_intra, int64_t *sends_inter)
+{
+    if (p < 1 || g < 1 || p % g != 0 || n < 0 || !valid_kind(dtype, op)) return -1;
+    for (int r = 0; r < p; r++)
+        if (!bufs[r] && n > 0) return -1;
+    if (n == 0 || p == 1) return 0;
+    const int m = p / g;
+    const int es = orc_elem_size(dtype);
+    const int hop_op = hop_of(op);
+    void **ptrs = (void **)malloc(sizeof(void *) * (size_t)p);
+    int64_t *tmp = (int64_t *)malloc(sizeof(int64_t) * (size_t)p);
+    int64_t *gb = (int64_t *)malloc(sizeof(int64_t) * (size_t)(g + 1));
+    int64_t *sb = (int64_t *)malloc(sizeof(int64_t) * (size_t)(m + 1));
+    if (!ptrs || !tmp || !gb || !sb) { free(ptrs); free(tmp); free(gb); free(sb); return -1; }
+
+    if (op == ORC_AVG_PREDIV)
+        for (int r = 0; r < p; r++)
+            for (int64_t i = 0; i < n; i++)
+                scale_by_inv_p(dtype, (unsigned char *)bufs[r] + (size_t)i * (size_t)es, p);
+
+    /* 1. reduce-scatter inside every node */
+    for (int j = 0; j < m; j++) {
+        for (int l = 0; l < g; l++) { ptrs[l] = bufs[j * g + l]; tmp[l] = 0; }
+        orc_ring_simulate(ptrs, g, n, dtype, hop_op, ORC_FORWARD, 0, g - 1, tmp);
+        if (sends_intra) for (int l = 0; l < g; l++) sends_intra[j * g + l] += tmp[l];
+    }
+    /* 2. all-reduce of every shard across the nodes */
+    orc_chunk_bounds(n, g, gb);
+    for (int l = 0; l < g; l++) {
+        const int c = (l + 1) % g;
+        const int64_t s0 = gb[c], len = gb[c + 1] - gb[c];
+        for (int j = 0; j < m; j++) {
+            ptrs[j] = (unsigned char *)bufs[j * g + l] + (size_t)s0 * (size_t)es;
+            tmp[j] = 0;
+        }
+        orc_ring_simulate(ptrs, m, len, dtype, hop_op, ORC_FORWARD, 0, m - 1, tmp);
+        if (op == ORC_AVG) {
+            /* the shard's owner scales by 1/p before the all-gather */
+            orc_chunk_bounds(len, m, sb);
+            for (int j = 0; j < m; j++) {
+                const int own = (j + 1) % m;
+                for (int64_t i = sb[own]; i < sb[own + 1]; i++)
+                    scale_by_inv_p(dtype, (unsigned char *)ptrs[j] + (size_t)i * (size_t)es, p);
+            }
+        }
+        orc_ring_simulate(ptrs, m, len, dtype, hop_op, ORC_FORWARD, m - 1, m - 1, tmp);
+        if (sends_inter) for (int j = 0; j < m; j++) sends_inter[j * g + l] += tmp[j];
+    }
+    /* 3. all-gather inside every node */
+    for (int j = 0; j < m; j++) {
+        for (int l = 0; l < g; l++) { ptrs[l] = bufs[j * g + l]; tmp[l] = 0; }
+        orc_ring_simulate(ptrs, g, n, dtype, hop_op, ORC_FORWARD, g - 1, g - 1, tmp);
+        if (sends_intra) for (int l = 0; l < g; l++) sends_intra[j * g + l] += tmp[l];
+    }
+    free(ptrs);
+    free(tmp);
+    free(gb);
+    free(sb);
+    return 0;
+}
+
+int orc_hier_fold_sampled(const void *vals, const int64_t *idx, int64_t m_samples,
+                          int p, int g, int64_t n, int dtype, int op, void *out)
+{
+    if (p < 1 || g < 1 || p % g != 0 || n < 0 || m_samples < 0 || !valid_kind(dtype, op)) return -1;
+    const int m = p / g;
+    const int es = orc_elem_size(dtype);
+    const int hop_op = hop_of(op);
+    const unsigned char *v = (const unsigned char *)vals;
+    unsigned char *o = (unsigned char *)out;
+    int64_t *gb = (int64_t *)malloc(sizeof(int64_t) * (size_t)(g + 1));
+    int64_t *sb = (int64_t *)malloc(sizeof(int64_t) * (size_t)(m + 1));
+    unsigned char *tmp = (unsigned char *)malloc((size_t)p * (size_t)es);
+    if (!gb || !sb || !tmp) { free(gb); free(sb); free(tmp); return -1; }
+    orc_chunk_bounds(n, g, gb);
+    int rc = 0;
+    for (int64_t jx = 0; jx < m_samples; jx++) {
+        const int64_t i = idx[jx];
+        if (i < 0 || i >= n) { rc = -1; break; }
+        for (int r = 0; r < p; r++) {
+            memcpy(tmp + (size_t)r * (size_t)es, v + ((size_t)r * (size_t)m_samples + (size_t)jx) * (size_t)es, (size_t)es);
+            if (op == ORC_AVG_PREDIV) scale_by_inv_p(dtype, tmp + (size_t)r * (size_t)es, p);
+        }
+        const int c = chunk_of(gb, g, i);
+        orc_chunk_bounds(gb[c + 1] - gb[c], m, sb);
+        const int s = chunk_of(sb, m, i - gb[c]);
+        unsigned char acc[4], part[4];
+        for (int t = 0; t < m; t++) {
+            const int node = (s + t) % m;
+            memcpy(part, tmp + (size_t)(node * g + c) * (size_t)es, (size_t)es);
+            for (int k = 1; k < g; k++)
+                orc_combine(dtype, hop_op, part, tmp + (size_t)(node * g + (c + k) % g) * (size_t)es, part);
+            if (t == 0) memcpy(acc, part, (size_t)es);
+            else orc_combine(dtype, hop_op, acc, part, acc);
+        }
+        if (op == ORC_AVG) scale_by_inv_p(dtype, acc, p);
+        memcpy(o + (size_t)jx * (size_t)es, acc, (size_t)es);
+    }
+    free(gb);
+    free(sb);
+    free(tmp);
+    return rc;
+}

@@ -107,6 +107,30 @@ int orc_fold_sampled(const void *vals, const int64_t *idx, int64_t m, int p,
  * simulator, in place. */
 int orc_tree_fold(void *const *bufs, int p, int64_t n, int dtype, int op);
 
+/* Hierarchical 2D all-reduce ("Ring All-Reduce, in depth", "What real
+ * libraries add" paragraph "Hierarchy", and "Worked example: flat versus
+ * hierarchical").  p = m * g ranks in m nodes of g; rank r = node * g + local.
+ *   1. reduce-scatter inside every node: a ring over its g ranks on
+ *      chunk_bounds(n, g); local rank l then holds its node's partial of
+ *      chunk (l + 1) mod g (its 1/g shard);
+ *   2. all-reduce of that shard across nodes, among the m ranks with the same
+ *      local rank: a ring over the nodes on chunk_bounds(shard, m); for avg
+ *      the owner scales by 1/p (p = all ranks) before this ring's all-gather;
+ *   3. all-gather inside every node.
+ * g == p is the flat ring; g == 1 is the flat ring run across the nodes.
+ * sends_intra / sends_inter (nullable, p entries): elements each rank sent
+ * within its node and across nodes.  Returns 0, or -1 on bad arguments
+ * (g < 1 or g not dividing p). */
+int orc_hier_simulate(void *const *bufs, int p, int g, int64_t n, int dtype,
+                      int op, int64_t *sends_intra, int64_t *sends_inter);
+
+/* Closed-form per-element fold of the hierarchical schedule, as
+ * orc_fold_sampled: element i of intra-node chunk c and shard sub-chunk s is
+ * sum over nodes s, s+1, ... (mod m) of each node's partial, the partial
+ * summing local ranks c, c+1, ... (mod g) of that node. */
+int orc_hier_fold_sampled(const void *vals, const int64_t *idx, int64_t m_samples,
+                          int p, int g, int64_t n, int dtype, int op, void *out);
+
 /* fp64 reference for float inputs: ref[i] = sum_r x_r[i] and
  * mag[i] = sum_r |x_r[i]| in double.  Inputs are f32/bf16/f16. */
 int orc_f64_sum(const void *const *bufs, int p, int64_t n, int dtype,

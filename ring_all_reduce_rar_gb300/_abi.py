@@ -44,12 +44,13 @@ class Options(ctypes.Structure):
         ("fault_rank", ctypes.c_int),
         ("fault_delay_ns", ctypes.c_uint),
         ("fused_path", ctypes.c_int),
+        ("hier_group", ctypes.c_int),
     ]
 
 
 def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, timeout_ns=0,
                  skip_pointer_check=False, fault_mode="none", fault_rank=0, fault_delay_ns=0,
-                 fused_path="auto") -> Options:
+                 fused_path="auto", hier_group=0) -> Options:
     o = Options()
     o.engine = ENGINE_CODES[engine] if isinstance(engine, str) else int(engine)
     o.channels = channels
@@ -61,6 +62,7 @@ def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, tim
     o.fault_rank = fault_rank
     o.fault_delay_ns = fault_delay_ns
     o.fused_path = FUSED_PATHS[fused_path] if isinstance(fused_path, str) else int(fused_path)
+    o.hier_group = hier_group
     return o
 
 

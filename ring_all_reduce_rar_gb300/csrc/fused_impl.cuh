@@ -271,6 +271,109 @@ __global__ void __launch_bounds__(kFusedThreads) fused_tree_order_kernel(const _
     }
 }
 
+// ---------------------------------------------------------------- hierarchical order
+//
+// "Ring All-Reduce, in depth", "Hierarchy": p = m nodes of g ranks
+// (rank = node * g + local); reduce-scatter inside the nodes on
+// chunk_bounds(n, g), all-reduce of every 1/g shard across the nodes on
+// chunk_bounds(shard, m), all-gather inside the nodes.  Element i of
+// intra-node chunk c and shard sub-chunk s therefore becomes the fold over
+// nodes s, s+1, ... (mod m) of node partials, each partial folding local
+// ranks c, c+1, ... (mod g) of its node.  avg scales the final value once.
+
+struct HierPos {
+    int c;  // intra-node chunk
+    int s;  // sub-chunk of that chunk across the nodes
+};
+
+__device__ __forceinline__ HierPos hier_pos(long long i, long long n, int g, int m) {
+    const long long gb = n / g, ge = n % g;
+    const int c = chunk_of(i, gb, ge);
+    const long long c0 = chunk_start(c, gb, ge);
+    const long long len = gb + (c < ge ? 1 : 0);
+    return HierPos{c, chunk_of(i - c0, len / m, len % m)};
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint4 hier_fold_vector(const FusedArgs &a, int p, int g, HierPos hp, long long v) {
+    constexpr int hop = HopOf<OP>::value;
+    const int m = p / g;
+    uint4 acc = make_uint4(0, 0, 0, 0);
+    for (int t = 0; t < m; t++) {
+        int node = hp.s + t;
+        node -= node >= m ? m : 0;
+        const int base = node * g;
+        uint4 part = make_uint4(0, 0, 0, 0);
+        for (int k0 = 0; k0 < g; k0 += 8) {
+            uint4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (k0 + j < g) {
+                    int l = hp.c + k0 + j;
+                    l -= l >= g ? g : 0;
+                    x[j] = contrib_vec<DT, OP>(__ldcs(reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, p, base + l)) + v),
+                                               a.inv_p);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                if (k0 + j < g) part = (k0 + j == 0) ? x[j] : hop_vec<DT, hop>(part, x[j]);
+        }
+        acc = t == 0 ? part : hop_vec<DT, hop>(acc, part);
+    }
+    if constexpr (OP == OP_AVG) acc = scale_vec<DT>(acc, a.inv_p);
+    return acc;
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t hier_fold_element(const FusedArgs &a, int p, int g, HierPos hp, long long i) {
+    constexpr int hop = HopOf<OP>::value;
+    const int m = p / g;
+    uint32_t acc = 0;
+    for (int t = 0; t < m; t++) {
+        int node = hp.s + t;
+        node -= node >= m ? m : 0;
+        uint32_t part = 0;
+        for (int k = 0; k < g; k++) {
+            int l = hp.c + k;
+            l -= l >= g ? g : 0;
+            const uint32_t x = contrib_word<DT, OP>(load_elem<DT>(rank_ptr(a.bufs, p, node * g + l), i), a.inv_p);
+            part = k == 0 ? x : hop_word<DT, hop>(part, x);
+        }
+        acc = t == 0 ? part : hop_word<DT, hop>(acc, part);
+    }
+    if constexpr (OP == OP_AVG) acc = scale_word<DT>(acc, a.inv_p);
+    return acc;
+}
+
+template <int DT, int OP, bool VEC>
+__global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel(const __grid_constant__ FusedArgs a, int g) {
+    const int p = a.p;
+    const int m = p / g;
+    const long long n = a.n;
+    constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
+    const long long nvec = (n + VE - 1) / VE;
+    const long long nfull = n / VE;
+    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (long long)gridDim.x * blockDim.x) {
+        const long long e0 = v * VE;
+        if (VEC && v < nfull) {
+            const HierPos a0 = hier_pos(e0, n, g, m), a1 = hier_pos(e0 + VE - 1, n, g, m);
+            if (a0.c == a1.c && a0.s == a1.s) {
+                const uint4 acc = hier_fold_vector<DT, OP>(a, p, g, a0, v);
+                for (int r = 0; r < p; r++) __stcs(reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, r)) + v, acc);
+                continue;
+            }
+        }
+        for (int l = 0; l < VE; l++) {
+            const long long i = e0 + l;
+            if (i >= n) break;
+            const uint32_t acc = hier_fold_element<DT, OP>(a, p, g, hier_pos(i, n, g, m), i);
+            for (int r = 0; r < p; r++) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- dispatch
 
 template <typename K>

@@ -157,6 +157,8 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.bufs.table = nullptr;
     a.n = (long long)n;
     a.p = p;
+    a.layout = RING_FLAT;
+    a.group = p;
     a.channels = G;
     a.fwd_channels = G;
     a.split = (long long)n;

@@ -15,6 +15,7 @@ namespace {
 using namespace rar;
 
 constexpr int kMaxRingCtas = 8192;           // flags / counters capacity
+constexpr int kRingPhases = 3;               // counter arrays: one per ring launch of a call
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr long long kMaxSlicesPerChannelStep = (1ll << 20) - 2;  // progress word field
 
@@ -38,11 +39,17 @@ struct rar_ctx {
     bool have_last = false;
     cudaStream_t last_stream = nullptr;
     bool last_ring = false;
-    unsigned last_epoch = 0;
-    unsigned last_status_epoch = 0;  // epoch of the last launch that can record a status (0: none)
+    // epochs of the last call's launches that can record a status: [lo, hi]
+    // (0, 0 when none can)
+    unsigned last_status_lo = 0;
+    unsigned last_status_hi = 0;
     int last_p = 0;
-    int last_channels = 0;
-    int last_fwd_channels = 0;
+    // ring launches of the last call (the hierarchical schedule makes three)
+    int last_phases = 0;
+    int last_layout[3] = {0, 0, 0};
+    int last_channels[3] = {0, 0, 0};
+    int last_fwd_channels[3] = {0, 0, 0};
+    int last_group = 0;
 };
 
 namespace {
@@ -84,6 +91,7 @@ int check_options(rar_ctx *h, const rar_options &o) {
     if (o.fault_mode < RAR_FAULT_NONE || o.fault_mode > RAR_FAULT_DELAY)
         return fail(h, RAR_EINVAL, "unknown fault_mode");
     if (o.fused_path < 0 || o.fused_path > 2) return fail(h, RAR_EINVAL, "unknown fused_path");
+    if (o.hier_group < 0 || o.hier_group > RAR_MAX_P) return fail(h, RAR_EINVAL, "hier_group out of range");
     return RAR_OK;
 }
 
@@ -157,6 +165,85 @@ bool all_aligned16(void *const *bufs, int p) {
     return true;
 }
 
+// One ring launch: `layout` picks the rings (flat; inside nodes of `group`;
+// across nodes), steps [first, first + steps) of that ring size, counters in
+// array `phase_idx`.  Channels and slices follow the tuned defaults unless
+// the options set them.
+int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dtype, int op, bool vec16, bool bidir,
+                      int layout, int group, int first, int steps, int phase_idx, cudaStream_t stream) {
+    const int threads = h->opt.block_threads ? h->opt.block_threads : 512;
+    if (threads > 512) return fail(h, RAR_EINVAL, "ring engines run at most 512 threads per CTA");
+    int per_sm = 0;
+    const int max_ctas = std::min(ring_max_coresident_ctas(dtype, op, vec16, threads, &per_sm), kMaxRingCtas);
+    // Defaults (from slice x channel x block sweeps on GB300): use every
+    // co-resident CTA, and give each channel one or a few large slices per
+    // step, since each slice hand-off costs a few microseconds.
+    int G = h->opt.channels;
+    if (G == 0) G = std::max(1, max_ctas / p);
+    if (bidir && G < 2) G = 2;
+    if ((long long)G * p > max_ctas) {
+        if (h->opt.channels) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
+        G = max_ctas / p;
+        if (G < (bidir ? 2 : 1))
+            return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
+    }
+    const long long split = bidir ? (long long)n - (long long)n / 2 : (long long)n;  // chunk_bounds(n, 2)
+    const int fwd_channels = bidir ? (G + 1) / 2 : G;
+    const int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
+    // the longest chunk any ring of this launch moves
+    const int rp = layout == RING_FLAT ? p : layout == RING_INTRA ? group : p / group;
+    const long long seg = layout == RING_INTER ? ((long long)n + group - 1) / group
+                                               : std::max(split, (long long)n - split);
+    const long long maxchunk = (seg + rp - 1) / rp;
+    long long slice = h->opt.slice_elems;
+    if (slice == 0) {
+        slice = (maxchunk + min_g - 1) / min_g;
+        slice = (slice + 1023) / 1024 * 1024;
+        slice = std::min<long long>(std::max<long long>(slice, 1024), 65536);
+    }
+    slice = std::max<long long>(16, (slice + 15) / 16 * 16);
+    while ((maxchunk + slice - 1) / slice / min_g > kMaxSlicesPerChannelStep) slice *= 2;
+
+    int rc = next_epoch(h, stream);
+    if (rc != RAR_OK) return rc;
+    RingArgs a;
+    a.bufs = ptrs;
+    a.n = (long long)n;
+    a.p = p;
+    a.layout = layout;
+    a.group = group;
+    a.channels = G;
+    a.fwd_channels = fwd_channels;
+    a.split = split;
+    a.slice = slice;
+    a.first_step = first;
+    a.n_steps = steps;
+    a.inv_p = 1.0f / (float)p;
+    a.epoch = h->epoch;
+    a.flags = h->flags;
+    a.recv_counts = h->recv_counts + (size_t)phase_idx * kMaxRingCtas;
+    a.status = h->status;
+    a.abort_word = h->abort_word;
+    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
+    a.fault_mode = h->opt.fault_mode;
+    a.fault_rank = h->opt.fault_rank;
+    a.fault_delay_ns = h->opt.fault_delay_ns;
+    cudaError_t ce = launch_ring(a, dtype, op, vec16, threads, stream);
+    if (ce != cudaSuccess) {
+        if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "ring grid cannot be co-resident");
+        return cuda_fail(h, ce, "launching the ring executor");
+    }
+    h->last_ring = true;
+    if (h->last_status_lo == 0) h->last_status_lo = h->epoch;
+    h->last_status_hi = h->epoch;
+    h->last_layout[phase_idx] = layout;
+    h->last_channels[phase_idx] = G;
+    h->last_fwd_channels[phase_idx] = fwd_channels;
+    h->last_group = group;
+    h->last_phases = phase_idx + 1;
+    return RAR_OK;
+}
+
 int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int phase, void *stream_v,
         bool host_mapped = false) {
     if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
@@ -167,7 +254,8 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     h->have_last = true;
     h->last_stream = stream;
     h->last_ring = false;
-    h->last_status_epoch = 0;
+    h->last_status_lo = h->last_status_hi = 0;
+    h->last_phases = 0;
     h->last_p = p;
     if (n == 0 || p == 1) return RAR_OK;
 
@@ -176,6 +264,10 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     const bool vec16 = all_aligned16(bufs, p);
     const float inv_p = 1.0f / (float)p;
     const int engine = h->opt.engine;
+    // hierarchical 2D schedule: nodes of `group` ranks (1 and p are the flat ring)
+    const int group = h->opt.hier_group;
+    const bool hier = group > 1 && group < p;
+    if (hier && p % group != 0) return fail(h, RAR_EINVAL, "hier_group must divide p");
 
     if (engine == RAR_ENGINE_FUSED || engine == RAR_ENGINE_FUSED_TREE) {
         FusedArgs a;
@@ -189,6 +281,15 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         a.epoch = 0;
         a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
         const bool tree = engine == RAR_ENGINE_FUSED_TREE && phase != PHASE_AG;
+        if (hier) {
+            if (engine != RAR_ENGINE_FUSED || phase != PHASE_ALL || h->opt.fused_path == 2)
+                return fail(h, RAR_EUNSUPPORTED,
+                            "the hierarchical order is offered for the full all-reduce on the fused engine's "
+                            "per-thread path and on the ring engine");
+            cudaError_t ce = launch_fused_hier(a, dtype, op, group, vec16, 256, stream);
+            if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the hierarchical fused kernel");
+            return RAR_OK;
+        }
         // data path: per-thread 128-bit loads ("registers") or the
         // rank-sequential bulk-copy streaming path.  Auto (measured on GB300):
         // registers for p <= 16 below 80 MB per rank, streaming otherwise.
@@ -214,7 +315,7 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
                 return fail(h, RAR_EINVAL, "streaming path: stages (channels) must be in [2, 8] and fit in 227 KB");
             cudaError_t ce = launch_fused_stream(a, dtype, op, (int)tb, stages, stream);
             if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the streaming fused kernel");
-            h->last_status_epoch = h->epoch;
+            h->last_status_lo = h->last_status_hi = h->epoch;
             return RAR_OK;
         }
         const int threads = 256;  // the fused kernels are compiled for 256 threads
@@ -225,71 +326,27 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
 
     // ---- ring engines
     const bool bidir = engine == RAR_ENGINE_RING_BIDIR;
-    const int threads = h->opt.block_threads ? h->opt.block_threads : 512;
-    if (threads > 512) return fail(h, RAR_EINVAL, "ring engines run at most 512 threads per CTA");
-    int per_sm = 0;
-    const int max_ctas = std::min(ring_max_coresident_ctas(dtype, op, vec16, threads, &per_sm), kMaxRingCtas);
-    // Defaults (from slice x channel x block sweeps on GB300): use every
-    // co-resident CTA, and give each channel one or a few large slices per
-    // step, since each slice hand-off costs a few microseconds.
-    int G = h->opt.channels;
-    if (G == 0) G = std::max(1, max_ctas / p);
-    if (bidir && G < 2) G = 2;
-    if ((long long)G * p > max_ctas) {
-        if (h->opt.channels) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
-        G = max_ctas / p;
-        if (G < (bidir ? 2 : 1))
-            return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
-    }
-    const long long split = bidir ? (long long)n - (long long)n / 2 : (long long)n;  // chunk_bounds(n, 2)
-    const int fwd_channels = bidir ? (G + 1) / 2 : G;
-    const int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
-    const long long maxchunk = (std::max(split, (long long)n - split) + p - 1) / p;
-    long long slice = h->opt.slice_elems;
-    if (slice == 0) {
-        slice = (maxchunk + min_g - 1) / min_g;
-        slice = (slice + 1023) / 1024 * 1024;
-        slice = std::min<long long>(std::max<long long>(slice, 1024), 65536);
-    }
-    slice = std::max<long long>(16, (slice + 15) / 16 * 16);
-    while ((maxchunk + slice - 1) / slice / min_g > kMaxSlicesPerChannelStep) slice *= 2;
-
-    RingArgs a;
-    rc = fill_ptrs(h, a.bufs, bufs, p, stream);
+    if (hier && (bidir || phase != PHASE_ALL))
+        return fail(h, RAR_EUNSUPPORTED, "the hierarchical ring runs the full all-reduce on the forward ring only");
+    RankPtrs ptrs;
+    rc = fill_ptrs(h, ptrs, bufs, p, stream);
     if (rc != RAR_OK) return rc;
-    rc = next_epoch(h, stream);
-    if (rc != RAR_OK) return rc;
-    a.n = (long long)n;
-    a.p = p;
-    a.channels = G;
-    a.fwd_channels = fwd_channels;
-    a.split = split;
-    a.slice = slice;
-    a.first_step = phase == PHASE_AG ? p - 1 : 0;
-    a.n_steps = phase == PHASE_ALL ? 2 * (p - 1) : p - 1;
-    a.inv_p = inv_p;
-    a.epoch = h->epoch;
-    a.flags = h->flags;
-    a.recv_counts = h->recv_counts;
-    a.status = h->status;
-    a.abort_word = h->abort_word;
-    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
-    a.fault_mode = h->opt.fault_mode;
-    a.fault_rank = h->opt.fault_rank;
-    a.fault_delay_ns = h->opt.fault_delay_ns;
-    cudaError_t ce = launch_ring(a, dtype, op, vec16, threads, stream);
-    if (ce != cudaSuccess) {
-        if (ce == cudaErrorCooperativeLaunchTooLarge) {
-            return fail(h, RAR_EUNSUPPORTED, "ring grid cannot be co-resident");
-        }
-        return cuda_fail(h, ce, "launching the ring executor");
+    if (!hier) {
+        const int first = phase == PHASE_AG ? p - 1 : 0;
+        const int steps = phase == PHASE_ALL ? 2 * (p - 1) : p - 1;
+        return launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, bidir, RING_FLAT, p, first, steps, 0, stream);
     }
-    h->last_ring = true;
-    h->last_epoch = h->epoch;
-    h->last_status_epoch = h->epoch;
-    h->last_channels = G;
-    h->last_fwd_channels = fwd_channels;
-    return RAR_OK;
+    // "Ring All-Reduce, in depth", "Hierarchy": reduce-scatter inside the
+    // nodes, all-reduce of each shard across the nodes, all-gather inside the
+    // nodes -- three launches in stream order
+    const int m = p / group;
+    rc = launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, false, RING_INTRA, group, 0, group - 1, 0, stream);
+    if (rc == RAR_OK)
+        rc = launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, false, RING_INTER, group, 0, 2 * (m - 1), 1, stream);
+    if (rc == RAR_OK)
+        rc = launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, false, RING_INTRA, group, group - 1, group - 1, 2,
+                               stream);
+    return rc;
 }
 
 }  // namespace
@@ -329,13 +386,13 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
     cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
     if (h->sm_count < 1) h->sm_count = 1;
     bool ok = cudaMalloc((void **)&h->flags, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
-              cudaMalloc((void **)&h->recv_counts, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+              cudaMalloc((void **)&h->recv_counts, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
               cudaMalloc((void **)&h->status, sizeof(RingStatus)) == cudaSuccess &&
               cudaMalloc((void **)&h->abort_word, sizeof(unsigned)) == cudaSuccess &&
               cudaMalloc((void **)&h->ptr_table, sizeof(void *) * RAR_MAX_P) == cudaSuccess;
     if (ok) {
         ok = cudaMemset(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
-             cudaMemset(h->recv_counts, 0, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+             cudaMemset(h->recv_counts, 0, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
              cudaMemset(h->status, 0, sizeof(RingStatus)) == cudaSuccess &&
              cudaMemset(h->abort_word, 0, sizeof(unsigned)) == cudaSuccess &&
              cudaDeviceSynchronize() == cudaSuccess;
@@ -429,11 +486,11 @@ int rar_status(rar_handle h) {
     DeviceGuard dg(h->device);
     cudaError_t ce = cudaStreamSynchronize(h->last_stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "synchronising the last call's stream");
-    if (h->last_status_epoch == 0) return RAR_OK;
+    if (h->last_status_lo == 0) return RAR_OK;
     RingStatus st{};
     ce = cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the status word");
-    if (st.epoch == h->last_status_epoch && st.code != 0) {
+    if (st.epoch >= h->last_status_lo && st.epoch <= h->last_status_hi && st.code != 0) {
         char buf[256];
         if (st.rank >= 0)
             std::snprintf(buf, sizeof(buf),
@@ -456,20 +513,29 @@ int rar_send_counts(rar_handle h, unsigned long long *out, int p) {
     int rc = rar_status(h);
     if (rc != RAR_OK && rc != RAR_ETIMEOUT) return rc;
     if (!h->last_ring) return RAR_OK;
-    const int G = h->last_channels;
-    std::vector<unsigned long long> rc_counts((size_t)p * (size_t)G);
     DeviceGuard dg(h->device);
-    cudaError_t ce = cudaMemcpy(rc_counts.data(), h->recv_counts, sizeof(unsigned long long) * rc_counts.size(),
-                                cudaMemcpyDeviceToHost);
-    if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the send counters");
-    // a CTA counts what it received; the sender is its left (forward ring)
-    // or right (mirrored ring) neighbour
-    for (int r = 0; r < p; r++)
-        for (int j = 0; j < G; j++) {
-            const bool fwd = j < h->last_fwd_channels;
-            const int sender = fwd ? (r + p - 1) % p : (r + 1) % p;
-            out[sender] += rc_counts[(size_t)r * G + j];
-        }
+    for (int ph = 0; ph < h->last_phases; ph++) {
+        const int G = h->last_channels[ph];
+        std::vector<unsigned long long> counts((size_t)p * (size_t)G);
+        cudaError_t ce = cudaMemcpy(counts.data(), h->recv_counts + (size_t)ph * kMaxRingCtas,
+                                    sizeof(unsigned long long) * counts.size(), cudaMemcpyDeviceToHost);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the send counters");
+        // a CTA counts what it received; the sender is its ring neighbour
+        const int g = h->last_group;
+        for (int r = 0; r < p; r++)
+            for (int j = 0; j < G; j++) {
+                int sender;
+                if (h->last_layout[ph] == RING_INTRA) {
+                    sender = r - r % g + (r % g + g - 1) % g;
+                } else if (h->last_layout[ph] == RING_INTER) {
+                    const int m = p / g;
+                    sender = ((r / g + m - 1) % m) * g + r % g;
+                } else {
+                    sender = j < h->last_fwd_channels[ph] ? (r + p - 1) % p : (r + 1) % p;
+                }
+                out[sender] += counts[(size_t)r * G + j];
+            }
+    }
     return RAR_OK;
 }
 

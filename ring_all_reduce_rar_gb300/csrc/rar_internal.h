@@ -51,11 +51,20 @@ struct FusedArgs {
     unsigned long long timeout_ns;
 };
 
+// Which rings a ring launch runs (the hierarchical schedule uses 1 and 2).
+enum RingLayout {
+    RING_FLAT = 0,   // one ring over all p ranks
+    RING_INTRA = 1,  // a ring inside each node of `group` consecutive ranks
+    RING_INTER = 2   // a ring across the nodes per local rank, on that rank's shard
+};
+
 // Ring engines: persistent cooperative launch of p * channels CTAs.
 struct RingArgs {
     RankPtrs bufs;
     long long n;
     int p;
+    int layout;          // RingLayout
+    int group;           // ranks per node (RING_INTRA / RING_INTER)
     int channels;        // CTAs per rank
     int fwd_channels;    // bidirectional: channels [0, fwd_channels) run the
                          // forward ring on the first half, the rest the
@@ -88,6 +97,9 @@ cudaError_t launch_ring(const RingArgs &a, int dtype, int op, bool vec16, int th
 // (n_stages + 2) tiles must fit in 227 KB of shared memory.
 cudaError_t launch_fused_stream(const FusedArgs &a, int dtype, int op, int tile_bytes, int n_stages,
                                 cudaStream_t stream);
+// Hierarchical order (nodes of g ranks, 1 < g < p, g | p), full all-reduce.
+cudaError_t launch_fused_hier(const FusedArgs &a, int dtype, int op, int g, bool vec16, int threads,
+                              cudaStream_t stream);
 // Largest co-resident grid for the ring kernel of this dtype/op (per device).
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
 // Co-resident CTAs per SM for a fused kernel instance.

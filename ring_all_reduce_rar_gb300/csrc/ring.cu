@@ -114,7 +114,7 @@ __device__ void ring_delay(unsigned ns) {
 // owner's avg scaling if `scale`.
 template <int DT, int OP, bool VEC>
 __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
-                                           bool scale, bool first_hop, float inv_p) {
+                                           bool scale, bool prescale_in, bool prescale_own, float inv_p) {
     constexpr int hop_op = HopOf<OP>::value;
     constexpr bool prediv = OP == OP_AVG_PREDIV;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
@@ -123,14 +123,14 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
     if (!VEC || vlo >= vhi) vlo = vhi = lo / VE;  // all of it on the element path
     const long long elo = VEC ? vlo * VE : lo;      // [lo, elo) and [ehi, hi) per element
     const long long ehi = VEC ? vhi * VE : lo;
-    // pre-divided average: the receiver's own element enters scaled, and so
-    // does the incoming one at reduce-scatter step 0 (the sender's original)
+    // pre-divided average: a rank's original element enters scaled -- the
+    // receiver's own, and the incoming one at reduce-scatter step 0
     auto one = [&](long long i) {
         uint32_t x = load_elem<DT>(src, i);
         if (reduce) {
-            if (prediv && first_hop) x = scale_word<DT>(x, inv_p);
+            if (prediv && prescale_in) x = scale_word<DT>(x, inv_p);
             uint32_t own = load_elem<DT>(dst, i);
-            if (prediv) own = scale_word<DT>(own, inv_p);
+            if (prediv && prescale_own) own = scale_word<DT>(own, inv_p);
             x = hop_word<DT, hop_op>(x, own);
         }
         if (OP == OP_AVG && scale) x = scale_word<DT>(x, inv_p);
@@ -164,8 +164,8 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
             if (vv < vhi) {
                 uint4 x = in[u];
                 if (reduce) {
-                    if (prediv && first_hop) x = scale_vec<DT>(x, inv_p);
-                    x = hop_vec<DT, hop_op>(x, prediv ? scale_vec<DT>(own[u], inv_p) : own[u]);
+                    if (prediv && prescale_in) x = scale_vec<DT>(x, inv_p);
+                    x = hop_vec<DT, hop_op>(x, (prediv && prescale_own) ? scale_vec<DT>(own[u], inv_p) : own[u]);
                 }
                 if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
                 d4[vv] = x;
@@ -183,29 +183,54 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
     const bool fwd = j < a.fwd_channels;
     const int jj = fwd ? j : j - a.fwd_channels;
     const int GG = fwd ? a.fwd_channels : a.channels - a.fwd_channels;
-    const long long seg_lo = fwd ? 0 : a.split;
-    const long long L = fwd ? a.split : a.n - a.split;
-    const int nb = fwd ? mod_p(r - 1, p) : mod_p(r + 1, p);  // the rank this CTA receives from
+    // this rank's ring: its size rp, its position in it, the global rank at
+    // a position, and the segment of the buffer the ring works on
+    int rp = p, pos = r, ring_base = 0, ring_step = 1;
+    long long seg_lo = fwd ? 0 : a.split;
+    long long L = fwd ? a.split : a.n - a.split;
+    if (a.layout == RING_INTRA) {
+        rp = a.group;
+        pos = r % a.group;
+        ring_base = r - pos;
+        seg_lo = 0;
+        L = a.n;
+    } else if (a.layout == RING_INTER) {
+        const int local = r % a.group;
+        rp = p / a.group;
+        pos = r / a.group;
+        ring_base = local;
+        ring_step = a.group;
+        const long long gb = a.n / a.group, ge = a.n % a.group;
+        const int c = local + 1 == a.group ? 0 : local + 1;  // the shard this rank owns after the intra ring
+        seg_lo = chunk_start(c, gb, ge);
+        L = gb + (c < ge ? 1 : 0);
+    }
+    const int nb_pos = fwd ? mod_p(pos - 1, rp) : mod_p(pos + 1, rp);
+    const int nb = ring_base + nb_pos * ring_step;  // the rank this CTA receives from
+    // avg scales once, at the final owner; pre-division scales each original
+    // contribution once, where it enters the reduction
+    const bool scale_here = OP == OP_AVG && a.layout != RING_INTRA;
+    const bool prediv_here = OP == OP_AVG_PREDIV && a.layout != RING_INTER;
     const char *src = rank_ptr(a.bufs, p, nb);
     char *dst = rank_ptr(a.bufs, p, r);
     unsigned long long *my_flag = a.flags + blockIdx.x;
     const unsigned long long *nb_flag = a.flags + (long long)nb * a.channels + j;
-    const long long base = L / p, extra = L % p;
+    const long long base = L / rp, extra = L % rp;
     unsigned long long received = 0;
     const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
     const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
 
     if (!muted) {
         for (int step = a.first_step; step < a.first_step + a.n_steps; step++) {
-            const bool rs = step < p - 1;
-            const int s = rs ? step : step - (p - 1);
+            const bool rs = step < rp - 1;
+            const int s = rs ? step : step - (rp - 1);
             int c;
-            if (fwd) c = rs ? mod_p(r - 1 - s, p) : mod_p(r - s, p);
-            else c = rs ? mod_p(r + 1 + s, p) : mod_p(r + s, p);
+            if (fwd) c = rs ? mod_p(pos - 1 - s, rp) : mod_p(pos - s, rp);
+            else c = rs ? mod_p(pos + 1 + s, rp) : mod_p(pos + s, rp);
             const long long cs = seg_lo + chunk_start(c, base, extra);
             const long long ce = seg_lo + chunk_start(c + 1, base, extra);
             const long long nsl = (ce - cs + a.slice - 1) / a.slice;
-            const bool scale = rs && s == p - 2;  // this rank becomes the chunk's owner
+            const bool scale = scale_here && rs && s == rp - 2;  // this rank becomes the chunk's owner
             long long loc = 0;
             for (long long sl = jj; sl < nsl; sl += GG, loc++) {
                 if (threadIdx.x == 0) {
@@ -222,7 +247,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
                 {
                     const long long lo = cs + sl * a.slice;
                     const long long hi = lo + a.slice < ce ? lo + a.slice : ce;
-                    ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale, rs && s == 0, a.inv_p);
+                    ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale, prediv_here && rs && s == 0, prediv_here,
+                                            a.inv_p);
                     received += (unsigned long long)(hi - lo);
                 }
                 __syncthreads();

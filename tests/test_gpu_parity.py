@@ -426,6 +426,62 @@ def test_tree_order_bit_exact_and_bound(rar, dev):
         assert np.all(np.abs(got - ref) <= 4 * p * 2.0 ** -24 * mag)
 
 
+# ----------------------------------------------------------------- hierarchical
+
+@pytest.mark.parametrize("engine", ["fused", "ring"])
+@pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "sum"), ("bfloat16", "avg"),
+                                      ("float32", "max"), ("float16", "avg_prediv"), ("int32", "sum")])
+def test_hierarchical_matches_oracle(rar, dev, engine, dtype, op):
+    """"Ring All-Reduce, in depth", "Hierarchy": the two-level schedule
+    (reduce-scatter in nodes, all-reduce of shards across nodes, all-gather
+    in nodes) against the oracle's composition of rings, bit for bit; the
+    ring engine's per-rank sends equal the oracle's intra + cross-node."""
+    dist = ("uniform_int", -(1 << 20), 21) if dtype == "int32" else ("normal", 1.0)
+    for p, g in [(4, 2), (8, 2), (8, 4), (16, 4), (64, 8)]:
+        n = p * 300 + 7
+        host = gen(p, n, dtype, dist, 1000 + p * g)
+        ref = [w.to_storage_numpy(t).copy() for t in host]
+        intra, inter = oracle.hier_simulate(ref, g, dtype, op)
+        _, rows = upload(host, dev)
+        with rar.Handle(0, engine=engine, hier_group=g) as h:
+            h.allreduce(rows, op=op)
+            h.check()
+            sends = h.send_counts(p)
+        torch.cuda.synchronize()
+        assert_bits_equal(rows, ref, f"{engine} hier p={p} g={g} {dtype} {op}")
+        if engine == "ring":
+            assert list(sends) == list(intra + inter)
+
+
+def test_hierarchical_degenerate_groups_are_flat(rar, dev):
+    p, n = 8, 8 * 123 + 5
+    host = gen(p, n, "bfloat16", ("normal", 1e-2), 5)
+    ref, _ = oracle_expect(host, "bfloat16", "sum", "ring")
+    for engine in ["fused", "ring"]:
+        for g in [1, p]:
+            _, rows = upload(host, dev)
+            with rar.Handle(0, engine=engine, hier_group=g) as h:
+                h.allreduce(rows)
+                h.check()
+            assert_bits_equal(rows, ref, f"{engine} g={g}")
+
+
+def test_hierarchical_rejections(rar, dev):
+    host = gen(8, 800, "float32", ("normal", 1.0), 6)
+    _, rows = upload(host, dev)
+    for opts, code in [(dict(engine="ring_bidir", hier_group=2), 2), (dict(engine="fused_tree", hier_group=2), 2),
+                       (dict(engine="fused", fused_path="stream", hier_group=2), 2),
+                       (dict(engine="ring", hier_group=3), 1)]:
+        with rar.Handle(0, **opts) as h:
+            with pytest.raises(rar.RarError) as e:
+                h.allreduce(rows)
+            assert e.value.code == code, opts
+    with rar.Handle(0, engine="ring", hier_group=2) as h:
+        with pytest.raises(rar.RarError) as e:
+            h.reduce_scatter(rows)
+        assert e.value.code == 2
+
+
 # ----------------------------------------------------------------- host buffers
 
 @pytest.mark.parametrize("engine", ["fused", "fused_stream", "ring"])

@@ -37,6 +37,11 @@
  *   RAR_ENGINE_FUSED_TREE  one kernel, tree order over the rank index (adjacent
  *                          pairs level by level); not bit-identical to the
  *                          ring, float sums within 4 p 2^-24 sum|x| of exact.
+ *   RAR_ENGINE_TREE        persistent executor of the tree all-reduce schedule
+ *                          ("Derive the cost of a ring all-reduce": reduce up a
+ *                          binary tree, broadcast down, 2 ceil(log2 p) steps);
+ *                          same arithmetic as RAR_ENGINE_FUSED_TREE; full
+ *                          all-reduce with sum, max or avg.
  *
  * Conventions for every call:
  *   - Return value: RAR_OK or a rar_status_code; rar_last_error(h) gives a
@@ -84,7 +89,8 @@ typedef enum {
     RAR_ENGINE_FUSED = 0,
     RAR_ENGINE_RING = 1,
     RAR_ENGINE_RING_BIDIR = 2,
-    RAR_ENGINE_FUSED_TREE = 3
+    RAR_ENGINE_FUSED_TREE = 3,
+    RAR_ENGINE_TREE = 4
 } rar_engine;
 
 typedef enum {

@@ -15,7 +15,7 @@ from . import _build
 
 DTYPE_CODES = {"int32": 0, "float32": 1, "bfloat16": 2, "float16": 3}
 OP_CODES = {"sum": 0, "max": 1, "avg": 2, "avg_prediv": 3}
-ENGINE_CODES = {"fused": 0, "ring": 1, "ring_bidir": 2, "fused_tree": 3}
+ENGINE_CODES = {"fused": 0, "ring": 1, "ring_bidir": 2, "fused_tree": 3, "tree": 4}
 FAULT_CODES = {"none": 0, "mute": 1, "delay": 2}
 FUSED_PATHS = {"auto": 0, "registers": 1, "stream": 2}
 STATUS_NAMES = {0: "RAR_OK", 1: "RAR_EINVAL", 2: "RAR_EUNSUPPORTED", 3: "RAR_ENOMEM",

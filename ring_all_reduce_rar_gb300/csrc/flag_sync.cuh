@@ -1,0 +1,88 @@
+// flag_sync.cuh -- progress words between CTA groups of one cooperative
+// launch (the ring and tree executors): release/acquire at GPU scope,
+// bounded waits, and the status word a wait that runs out fills in.
+//
+// A CTA publishes its progress after each slice with a release store of a
+// 64-bit word (epoch << 32) | (step << 20) | (slice-within-channel + 1); a
+// waiter acquires it.  Epoch-tagged words need no reset between calls.
+// Every wait is bounded by the call's timeout (globaltimer) and an
+// iteration cap; the first CTA to give up records where, raises the abort
+// word (which every other wait polls) and returns.  Nothing traps.
+#pragma once
+
+#include "elem_ops.cuh"
+
+namespace rar {
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned long long progress_tag(unsigned epoch, int step, long long loc) {
+    return ((unsigned long long)epoch << 32) | ((unsigned long long)step << 20) | (unsigned long long)(loc + 1);
+}
+
+__device__ __forceinline__ int mod_p(int v, int p) {
+    v %= p;
+    return v < 0 ? v + p : v;
+}
+
+// Record a timeout (first CTA of this call only) and raise the abort word.
+static __device__ void ring_give_up(const RingArgs &a, int rank, int step, long long slice, int nb,
+                             unsigned long long seen, unsigned long long wanted) {
+    unsigned prev = atomicMax(&a.status->epoch, a.epoch);
+    if (prev < a.epoch) {
+        a.status->code = RAR_ETIMEOUT;
+        a.status->rank = rank;
+        a.status->step = step;
+        a.status->slice = (int)slice;
+        a.status->waited_on = nb;
+        a.status->flag_seen = seen;
+        a.status->flag_wanted = wanted;
+        __threadfence();
+    }
+    atomicMax(a.abort_word, a.epoch);
+}
+
+// Bounded acquire-wait for the neighbour's progress word.  Returns false if
+// the wait ran out or another CTA aborted the call.
+static __device__ bool ring_wait(const RingArgs &a, const unsigned long long *flag, unsigned long long target, int rank,
+                          int step, long long slice, int nb) {
+    unsigned long long v = ld_acquire_u64(flag);
+    if (v >= target) return true;
+    const unsigned long long t0 = global_ns();
+    const unsigned long long max_iters = a.timeout_ns / 16ull + (1ull << 20);
+    for (unsigned long long it = 0;; it++) {
+        __nanosleep(32);
+        v = ld_acquire_u64(flag);
+        if (v >= target) return true;
+        if (ld_relaxed_u32(a.abort_word) == a.epoch) return false;
+        if (it >= max_iters || global_ns() - t0 > a.timeout_ns) {
+            ring_give_up(a, rank, step, slice, nb, v, target);
+            return false;
+        }
+    }
+}
+
+// Injected straggler: pause about `ns` (bounded by the same clock).
+static __device__ void ring_delay(unsigned ns) {
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < (1 << 22) && global_ns() - t0 < ns; it++) __nanosleep(256);
+}
+
+}  // namespace rar

@@ -82,7 +82,7 @@ struct DeviceGuard {
 };
 
 int check_options(rar_ctx *h, const rar_options &o) {
-    if (o.engine < RAR_ENGINE_FUSED || o.engine > RAR_ENGINE_FUSED_TREE)
+    if (o.engine < RAR_ENGINE_FUSED || o.engine > RAR_ENGINE_TREE)
         return fail(h, RAR_EINVAL, "unknown engine");
     if (o.channels < 0 || o.slice_elems < 0 || o.block_threads < 0)
         return fail(h, RAR_EINVAL, "negative channels, slice_elems or block_threads");
@@ -244,6 +244,66 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dty
     return RAR_OK;
 }
 
+// The tree executor: every co-resident CTA, slices of about n / channels.
+int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dtype, int op, bool vec16,
+                         cudaStream_t stream) {
+    const int threads = h->opt.block_threads ? h->opt.block_threads : 512;
+    if (threads > 512) return fail(h, RAR_EINVAL, "the tree executor runs at most 512 threads per CTA");
+    const int max_ctas = std::min(tree_max_coresident_ctas(dtype, op, vec16, threads), kMaxRingCtas);
+    int G = h->opt.channels ? h->opt.channels : std::max(1, max_ctas / p);
+    if ((long long)G * p > max_ctas) {
+        if (h->opt.channels) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
+        G = max_ctas / p;
+        if (G < 1) return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
+    }
+    long long slice = h->opt.slice_elems;
+    if (slice == 0) {
+        slice = ((long long)n + G - 1) / G;
+        slice = std::min<long long>(std::max<long long>((slice + 1023) / 1024 * 1024, 1024), 65536);
+    }
+    slice = std::max<long long>(16, (slice + 15) / 16 * 16);
+    while (((long long)n + slice - 1) / slice / G > kMaxSlicesPerChannelStep - 1) slice *= 2;
+    int rc = next_epoch(h, stream);
+    if (rc != RAR_OK) return rc;
+    cudaError_t ce = cudaMemsetAsync(h->recv_counts, 0, sizeof(unsigned long long) * (size_t)p, stream);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the send counters");
+    RingArgs a;
+    a.bufs = ptrs;
+    a.n = (long long)n;
+    a.p = p;
+    a.layout = TREE;
+    a.group = p;
+    a.channels = G;
+    a.fwd_channels = G;
+    a.split = (long long)n;
+    a.slice = slice;
+    a.first_step = 0;
+    a.n_steps = 0;
+    a.inv_p = 1.0f / (float)p;
+    a.epoch = h->epoch;
+    a.flags = h->flags;
+    a.recv_counts = h->recv_counts;
+    a.status = h->status;
+    a.abort_word = h->abort_word;
+    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
+    a.fault_mode = h->opt.fault_mode;
+    a.fault_rank = h->opt.fault_rank;
+    a.fault_delay_ns = h->opt.fault_delay_ns;
+    ce = launch_tree(a, dtype, op, vec16, threads, stream);
+    if (ce != cudaSuccess) {
+        if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "tree grid cannot be co-resident");
+        return cuda_fail(h, ce, "launching the tree executor");
+    }
+    h->last_ring = true;
+    h->last_status_lo = h->last_status_hi = h->epoch;
+    h->last_layout[0] = TREE;
+    h->last_channels[0] = G;
+    h->last_fwd_channels[0] = G;
+    h->last_group = p;
+    h->last_phases = 1;
+    return RAR_OK;
+}
+
 int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int phase, void *stream_v,
         bool host_mapped = false) {
     if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
@@ -322,6 +382,15 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         cudaError_t ce = launch_fused(a, dtype, op, tree, vec16, threads, 0, stream);
         if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the fused kernel");
         return RAR_OK;
+    }
+
+    if (engine == RAR_ENGINE_TREE) {
+        if (phase != PHASE_ALL || hier || op == RAR_AVG_PREDIV)
+            return fail(h, RAR_EUNSUPPORTED, "the tree executor runs the full all-reduce with sum, max or avg");
+        RankPtrs ptrs;
+        rc = fill_ptrs(h, ptrs, bufs, p, stream);
+        if (rc != RAR_OK) return rc;
+        return launch_tree_schedule(h, ptrs, p, n, dtype, op, vec16, stream);
     }
 
     // ---- ring engines
@@ -514,6 +583,15 @@ int rar_send_counts(rar_handle h, unsigned long long *out, int p) {
     if (rc != RAR_OK && rc != RAR_ETIMEOUT) return rc;
     if (!h->last_ring) return RAR_OK;
     DeviceGuard dg(h->device);
+    if (h->last_layout[0] == TREE) {
+        // the tree executor counts per sender directly
+        std::vector<unsigned long long> counts((size_t)p);
+        cudaError_t ce =
+            cudaMemcpy(counts.data(), h->recv_counts, sizeof(unsigned long long) * (size_t)p, cudaMemcpyDeviceToHost);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the send counters");
+        for (int r = 0; r < p; r++) out[r] = counts[(size_t)r];
+        return RAR_OK;
+    }
     for (int ph = 0; ph < h->last_phases; ph++) {
         const int G = h->last_channels[ph];
         std::vector<unsigned long long> counts((size_t)p * (size_t)G);

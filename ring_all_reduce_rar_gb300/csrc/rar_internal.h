@@ -55,7 +55,8 @@ struct FusedArgs {
 enum RingLayout {
     RING_FLAT = 0,   // one ring over all p ranks
     RING_INTRA = 1,  // a ring inside each node of `group` consecutive ranks
-    RING_INTER = 2   // a ring across the nodes per local rank, on that rank's shard
+    RING_INTER = 2,  // a ring across the nodes per local rank, on that rank's shard
+    TREE = 3         // the tree executor (tree.cu); its counters are per sender
 };
 
 // Ring engines: persistent cooperative launch of p * channels CTAs.
@@ -100,6 +101,10 @@ cudaError_t launch_fused_stream(const FusedArgs &a, int dtype, int op, int tile_
 // Hierarchical order (nodes of g ranks, 1 < g < p, g | p), full all-reduce.
 cudaError_t launch_fused_hier(const FusedArgs &a, int dtype, int op, int g, bool vec16, int threads,
                               cudaStream_t stream);
+// Tree executor (tree.cu): full all-reduce; a.recv_counts holds p per-rank
+// send counters, zeroed by the caller before the launch.
+cudaError_t launch_tree(const RingArgs &a, int dtype, int op, bool vec16, int threads, cudaStream_t stream);
+int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads);
 // Largest co-resident grid for the ring kernel of this dtype/op (per device).
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
 // Co-resident CTAs per SM for a fused kernel instance.

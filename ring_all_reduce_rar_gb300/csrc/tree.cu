@@ -1,0 +1,197 @@
+// tree.cu -- the tree all-reduce schedule as a persistent executor.
+//
+// "Derive the cost of a ring all-reduce" compares the ring with a tree
+// all-reduce: a reduce up a binary tree and a broadcast down, about
+// 2 log2(n) steps instead of 2(n - 1), so fewer step latencies on small
+// buffers.  Here p rank groups of `channels` CTAs (one cooperative launch)
+// run L = ceil(log2 p) reduce levels and L broadcast levels over the whole
+// buffer, slice-pipelined like the ring executor:
+//   reduce level l:    rank r with r mod 2^(l+1) == 0 and r + 2^l < p
+//                      combines its child's buffer into its own:
+//                      own = op(own, child) (lower rank index on the left);
+//   broadcast level l: (from l = L - 1 down to 0) rank c with
+//                      c mod 2^(l+1) == 2^l copies its parent c - 2^l.
+// The reduce folds in exactly the tree order of the fused tree mode (adjacent
+// pairs level by level, an odd last rank carried up), so the result equals
+// that order bit for bit.  avg is scaled by the root after its last level.
+// Element moves: (p - 1) reduce hops of 3 moves and (p - 1) broadcast hops of
+// 2, the same 5 (p - 1) n as the ring.
+//
+// Hand-offs use the progress words of flag_sync.cuh; a rank with nothing to
+// do at a step publishes the step as passed so that waiters move on.  Every
+// wait is bounded.
+#include "flag_sync.cuh"
+
+namespace rar {
+
+constexpr int kTreeThreads = 512;
+constexpr long long kTreePassLoc = (1ll << 20) - 2;  // "whole step passed"
+
+// One slice [lo, hi): reduce: dst = op(dst, src) (+ the root's avg scaling);
+// broadcast: dst = src.
+template <int DT, int OP, bool VEC>
+__device__ __forceinline__ void tree_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
+                                           bool scale, float inv_p) {
+    constexpr int hop_op = HopOf<OP>::value;
+    constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
+    const int T = blockDim.x;
+    auto one = [&](long long i) {
+        uint32_t x = load_elem<DT>(src, i);
+        if (reduce) x = hop_word<DT, hop_op>(load_elem<DT>(dst, i), x);
+        if (OP == OP_AVG && scale) x = scale_word<DT>(x, inv_p);
+        store_elem<DT>(dst, i, x);
+    };
+    long long vlo = (lo + VE - 1) / VE, vhi = hi / VE;
+    if (!VEC || vlo >= vhi) {
+        for (long long i = lo + threadIdx.x; i < hi; i += T) one(i);
+        return;
+    }
+    for (long long i = lo + threadIdx.x; i < vlo * VE; i += T) one(i);
+    for (long long i = vhi * VE + threadIdx.x; i < hi; i += T) one(i);
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    for (long long v = vlo + threadIdx.x; v < vhi; v += T) {
+        uint4 x = __ldcg(s4 + v);
+        if (reduce) x = hop_vec<DT, hop_op>(__ldcs(d4 + v), x);
+        if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
+        d4[v] = x;
+    }
+}
+
+template <int DT, int OP, bool VEC>
+__global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __grid_constant__ RingArgs a) {
+    __shared__ int s_stop;
+    const int p = a.p;
+    const int r = blockIdx.x / a.channels;
+    const int j = blockIdx.x % a.channels;
+    int L = 0;
+    while ((1 << L) < p) L++;
+    char *mine = rank_ptr(a.bufs, p, r);
+    unsigned long long *my_flag = a.flags + blockIdx.x;
+    const long long nsl = (a.n + a.slice - 1) / a.slice;
+    const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
+    const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
+    if (muted) return;
+
+    for (int t = 0; t < 2 * L; t++) {
+        const bool up = t < L;
+        const int l = up ? t : 2 * L - 1 - t;
+        const int span = 1 << l;
+        int peer = -1;  // the rank read at this step
+        if (up) {
+            if ((r & (2 * span - 1)) == 0 && r + span < p) peer = r + span;
+        } else {
+            if ((r & (2 * span - 1)) == span) peer = r - span;
+        }
+        if (peer < 0) {
+            // nothing to do: the step is passed as soon as the previous one is
+            if (threadIdx.x == 0) {
+                __threadfence();
+                st_release_u64(my_flag, progress_tag(a.epoch, t, kTreePassLoc));
+            }
+            continue;
+        }
+        const char *src = rank_ptr(a.bufs, p, peer);
+        const unsigned long long *peer_flag = a.flags + (long long)peer * a.channels + j;
+        const bool root_last = up && r == 0 && l == L - 1;
+        long long loc = 0;
+        for (long long sl = j; sl < nsl; sl += a.channels, loc++) {
+            if (threadIdx.x == 0) {
+                // the peer's data is final for this slice once it passed step t - 1
+                bool ok = t > 0 ? ring_wait(a, peer_flag, progress_tag(a.epoch, t - 1, loc), r, t, sl, peer)
+                                : ld_relaxed_u32(a.abort_word) != a.epoch;
+                if (ok && slow) ring_delay(a.fault_delay_ns);
+                s_stop = ok ? 0 : 1;
+            }
+            __syncthreads();
+            if (s_stop) return;
+            const long long lo = sl * a.slice;
+            const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
+            tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, root_last, a.inv_p);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // elements the peer sent
+                __threadfence();
+                st_release_u64(my_flag, progress_tag(a.epoch, t, loc));
+            }
+        }
+    }
+}
+
+template <int DT, int OP, bool VEC>
+static cudaError_t launch_tree_t(const RingArgs &a, int threads, cudaStream_t stream) {
+    void *args[] = {const_cast<RingArgs *>(&a)};
+    return cudaLaunchCooperativeKernel((const void *)tree_executor_kernel<DT, OP, VEC>,
+                                       dim3((unsigned)(a.p * a.channels)), dim3((unsigned)threads), args, 0, stream);
+}
+
+template <int DT, int OP>
+static cudaError_t launch_tree_op(const RingArgs &a, bool vec16, int threads, cudaStream_t stream) {
+    return vec16 ? launch_tree_t<DT, OP, true>(a, threads, stream) : launch_tree_t<DT, OP, false>(a, threads, stream);
+}
+
+cudaError_t launch_tree(const RingArgs &a, int dtype, int op, bool vec16, int threads, cudaStream_t stream) {
+    switch (dtype) {
+    case DT_I32:
+        if (op == OP_SUM) return launch_tree_op<DT_I32, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_tree_op<DT_I32, OP_MAX>(a, vec16, threads, stream);
+        break;
+    case DT_F32:
+        if (op == OP_SUM) return launch_tree_op<DT_F32, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_tree_op<DT_F32, OP_MAX>(a, vec16, threads, stream);
+        if (op == OP_AVG) return launch_tree_op<DT_F32, OP_AVG>(a, vec16, threads, stream);
+        break;
+    case DT_BF16:
+        if (op == OP_SUM) return launch_tree_op<DT_BF16, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_tree_op<DT_BF16, OP_MAX>(a, vec16, threads, stream);
+        if (op == OP_AVG) return launch_tree_op<DT_BF16, OP_AVG>(a, vec16, threads, stream);
+        break;
+    case DT_F16:
+        if (op == OP_SUM) return launch_tree_op<DT_F16, OP_SUM>(a, vec16, threads, stream);
+        if (op == OP_MAX) return launch_tree_op<DT_F16, OP_MAX>(a, vec16, threads, stream);
+        if (op == OP_AVG) return launch_tree_op<DT_F16, OP_AVG>(a, vec16, threads, stream);
+        break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename K>
+static int tree_occ_of(K kernel, int threads) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess) return 0;
+    return nb;
+}
+
+template <int DT, int OP>
+static int tree_occ(bool vec16, int threads) {
+    return vec16 ? tree_occ_of(tree_executor_kernel<DT, OP, true>, threads)
+                 : tree_occ_of(tree_executor_kernel<DT, OP, false>, threads);
+}
+
+int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads) {
+    int per_sm = 0;
+    switch (dtype) {
+    case DT_I32: per_sm = op == OP_SUM ? tree_occ<DT_I32, OP_SUM>(vec16, threads) : tree_occ<DT_I32, OP_MAX>(vec16, threads); break;
+    case DT_F32:
+        per_sm = op == OP_SUM ? tree_occ<DT_F32, OP_SUM>(vec16, threads)
+                 : op == OP_MAX ? tree_occ<DT_F32, OP_MAX>(vec16, threads)
+                                : tree_occ<DT_F32, OP_AVG>(vec16, threads);
+        break;
+    case DT_BF16:
+        per_sm = op == OP_SUM ? tree_occ<DT_BF16, OP_SUM>(vec16, threads)
+                 : op == OP_MAX ? tree_occ<DT_BF16, OP_MAX>(vec16, threads)
+                                : tree_occ<DT_BF16, OP_AVG>(vec16, threads);
+        break;
+    default:
+        per_sm = op == OP_SUM ? tree_occ<DT_F16, OP_SUM>(vec16, threads)
+                 : op == OP_MAX ? tree_occ<DT_F16, OP_MAX>(vec16, threads)
+                                : tree_occ<DT_F16, OP_AVG>(vec16, threads);
+        break;
+    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return per_sm * sms;
+}
+
+}  // namespace rar

@@ -482,6 +482,61 @@ def test_hierarchical_rejections(rar, dev):
         assert e.value.code == 2
 
 
+# ----------------------------------------------------------------- tree executor
+
+def _tree_children(r, p):
+    L = max(1, (p - 1).bit_length())
+    kids = []
+    for l in range(L):
+        span = 1 << l
+        if r % (2 * span) == 0 and r + span < p:
+            kids.append(r + span)
+    return kids
+
+
+@pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "sum"), ("float16", "avg"),
+                                      ("float32", "max"), ("int32", "sum"), ("bfloat16", "avg")])
+def test_tree_executor_matches_tree_order(rar, dev, dtype, op):
+    """"Derive the cost of a ring all-reduce": reduce up a binary tree,
+    broadcast down.  The executor folds in the oracle's tree order bit for
+    bit; every non-root rank sends n up once and n to each child."""
+    dist = ("uniform_int", -(1 << 20), 21) if dtype == "int32" else ("normal", 1.0)
+    for p in [2, 3, 4, 5, 7, 8, 13, 16, 64]:
+        for n in [1, p + 3, 4099, 64 * 1000 + 5]:
+            host = gen(p, n, dtype, dist, 300 + p * 7 + n)
+            ref = [w.to_storage_numpy(t).copy() for t in host]
+            oracle.tree_fold(ref, dtype, op)
+            _, rows = upload(host, dev)
+            with rar.Handle(0, engine="tree") as h:
+                h.allreduce(rows, op=op)
+                h.check()
+                sends = h.send_counts(p)
+            torch.cuda.synchronize()
+            assert_bits_equal(rows, ref, f"tree p={p} n={n} {dtype} {op}")
+            expect = [(n if r else 0) + n * len(_tree_children(r, p)) for r in range(p)]
+            assert list(sends) == expect
+            assert sum(sends) == 2 * (p - 1) * n
+
+
+def test_tree_executor_fault_and_rejections(rar, dev):
+    host = gen(8, 8 * 4096, "float32", ("normal", 1.0), 8)
+    _, rows = upload(host, dev)
+    with rar.Handle(0, engine="tree", timeout_ns=50_000_000, fault_mode="mute", fault_rank=2) as h:
+        # rank 2 is waited on by rank 0 at level 1 (a muted leaf such as rank 1
+        # stalls nobody: its data is only read at step 0, which has no wait)
+        h.allreduce(rows)
+        assert h.status() == 5
+    for fn, kw in [("reduce_scatter", {}), ("allreduce", dict(op="avg_prediv"))]:
+        with rar.Handle(0, engine="tree") as h:
+            with pytest.raises(rar.RarError) as e:
+                getattr(h, fn)(rows, **kw)
+            assert e.value.code == 2
+    with rar.Handle(0, engine="tree", hier_group=2) as h:
+        with pytest.raises(rar.RarError) as e:
+            h.allreduce(rows)
+        assert e.value.code == 2
+
+
 # ----------------------------------------------------------------- host buffers
 
 @pytest.mark.parametrize("engine", ["fused", "fused_stream", "ring"])

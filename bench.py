@@ -325,6 +325,49 @@ def run_ours(args):
     ctx.close()
 
 
+# ------------------------------------------------------------------ size sweep
+
+def run_sweep(args):
+    """Device time per call across message sizes (the p = 16 sweep workload),
+    one JSON line per (engine, size).  The GPU is first held by a short sleep
+    kernel so that the host can queue K calls ahead; CUDA events around the K
+    calls then time back-to-back device execution, not host call overhead."""
+    import ring_all_reduce_rar_gb300 as rar
+    rar.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dtype, op, dist = w.SWEEP_PAIRS[args.pair]
+    p = w.SWEEP_P
+    e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
+    engines = ["fused", "ring", "ring_bidir", "tree"] if args.engine == "all" else [args.engine]
+    for n in w.SWEEP_SIZES:
+        _, rows = w.make_inputs(p, n, dtype, dist, w.seed_of(w.SWEEP_INDEX), device=dev)
+        k = 200 if n <= 4 ** 9 else 20
+        for eng in engines:
+            if eng == "tree" and op == "avg_prediv":
+                continue
+            with rar.Handle(0, engine=eng, skip_pointer_check=True) as h:
+                for _ in range(3):
+                    h.allreduce(rows, op=op)
+                h.check()
+                torch.cuda.synchronize()
+                torch.cuda._sleep(200_000_000)  # ~0.1 s of GPU time to queue behind
+                start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                start.record()
+                for _ in range(k):
+                    h.allreduce(rows, op=op)
+                end.record()
+                torch.cuda.synchronize()
+                assert h.status() == 0
+                us = start.elapsed_time(end) * 1e3 / k
+            rb = (2 * p * n * e) if eng == "fused" else 5 * (p - 1) * n * e
+            print(json.dumps({"sweep": f"p{p}_{dtype}_{op}", "engine": eng, "n": n, "us_per_call": round(us, 2),
+                              "algbw_gbs": round(p * n * e / us / 1e3, 2),
+                              "roofline_frac": round(rb / us / 1e3 / hbm_peak()[0], 4)}), flush=True)
+        del rows
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -369,7 +412,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--engine", choices=["fused", "ring", "ring_bidir", "fused_tree", "all"], default="all")
+    ap.add_argument("--engine", choices=["fused", "ring", "ring_bidir", "fused_tree", "tree", "all"], default="all")
+    ap.add_argument("--sweep", action="store_true",
+                    help="device time per call over the p = 16 message-size sweep (not the benchmark line)")
+    ap.add_argument("--pair", type=int, default=0, help="--sweep: dtype/op pair of the sweep workload (0..2)")
     ap.add_argument("--workload", choices=sorted(w.WORKLOADS), default="p8_n1073741824_bf16")
     ap.add_argument("--op", choices=["sum", "avg", "max"], default=None)
     ap.add_argument("--n", type=int, default=None,
@@ -378,7 +424,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

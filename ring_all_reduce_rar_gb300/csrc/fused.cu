@@ -4,30 +4,30 @@
 
 namespace rar {
 
-cudaError_t launch_fused(const FusedArgs &a, int dtype, int op, bool tree, bool vec16, int threads, int grid_cap,
+cudaError_t launch_fused(const FusedArgs &a, int dtype, int op, bool tree, bool vec16, int threads,
                          cudaStream_t stream) {
     switch (dtype) {
     case DT_I32:
-        if (op == OP_SUM) return launch_fused_op<DT_I32, OP_SUM>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_I32, OP_MAX>(a, tree, vec16, threads, grid_cap, stream);
+        if (op == OP_SUM) return launch_fused_op<DT_I32, OP_SUM>(a, tree, vec16, threads, stream);
+        if (op == OP_MAX) return launch_fused_op<DT_I32, OP_MAX>(a, tree, vec16, threads, stream);
         break;
     case DT_F32:
-        if (op == OP_SUM) return launch_fused_op<DT_F32, OP_SUM>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_F32, OP_MAX>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_AVG) return launch_fused_op<DT_F32, OP_AVG>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_F32, OP_AVG_PREDIV>(a, tree, vec16, threads, grid_cap, stream);
+        if (op == OP_SUM) return launch_fused_op<DT_F32, OP_SUM>(a, tree, vec16, threads, stream);
+        if (op == OP_MAX) return launch_fused_op<DT_F32, OP_MAX>(a, tree, vec16, threads, stream);
+        if (op == OP_AVG) return launch_fused_op<DT_F32, OP_AVG>(a, tree, vec16, threads, stream);
+        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_F32, OP_AVG_PREDIV>(a, tree, vec16, threads, stream);
         break;
     case DT_BF16:
-        if (op == OP_SUM) return launch_fused_op<DT_BF16, OP_SUM>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_BF16, OP_MAX>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_AVG) return launch_fused_op<DT_BF16, OP_AVG>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_BF16, OP_AVG_PREDIV>(a, tree, vec16, threads, grid_cap, stream);
+        if (op == OP_SUM) return launch_fused_op<DT_BF16, OP_SUM>(a, tree, vec16, threads, stream);
+        if (op == OP_MAX) return launch_fused_op<DT_BF16, OP_MAX>(a, tree, vec16, threads, stream);
+        if (op == OP_AVG) return launch_fused_op<DT_BF16, OP_AVG>(a, tree, vec16, threads, stream);
+        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_BF16, OP_AVG_PREDIV>(a, tree, vec16, threads, stream);
         break;
     case DT_F16:
-        if (op == OP_SUM) return launch_fused_op<DT_F16, OP_SUM>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_F16, OP_MAX>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_AVG) return launch_fused_op<DT_F16, OP_AVG>(a, tree, vec16, threads, grid_cap, stream);
-        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_F16, OP_AVG_PREDIV>(a, tree, vec16, threads, grid_cap, stream);
+        if (op == OP_SUM) return launch_fused_op<DT_F16, OP_SUM>(a, tree, vec16, threads, stream);
+        if (op == OP_MAX) return launch_fused_op<DT_F16, OP_MAX>(a, tree, vec16, threads, stream);
+        if (op == OP_AVG) return launch_fused_op<DT_F16, OP_AVG>(a, tree, vec16, threads, stream);
+        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_F16, OP_AVG_PREDIV>(a, tree, vec16, threads, stream);
         break;
     }
     return cudaErrorInvalidValue;
@@ -75,29 +75,6 @@ cudaError_t launch_fused_hier(const FusedArgs &a, int dtype, int op, int g, bool
         break;
     }
     return cudaErrorInvalidValue;
-}
-
-int fused_blocks_per_sm(int dtype, int op, bool tree, bool vec16, int p, int threads) {
-    switch (dtype) {
-    case DT_I32:
-        return op == OP_SUM ? fused_occ_op<DT_I32, OP_SUM>(tree, vec16, p, threads)
-                            : fused_occ_op<DT_I32, OP_MAX>(tree, vec16, p, threads);
-    case DT_F32:
-        return op == OP_SUM ? fused_occ_op<DT_F32, OP_SUM>(tree, vec16, p, threads)
-               : op == OP_MAX ? fused_occ_op<DT_F32, OP_MAX>(tree, vec16, p, threads)
-               : op == OP_AVG ? fused_occ_op<DT_F32, OP_AVG>(tree, vec16, p, threads)
-                              : fused_occ_op<DT_F32, OP_AVG_PREDIV>(tree, vec16, p, threads);
-    case DT_BF16:
-        return op == OP_SUM ? fused_occ_op<DT_BF16, OP_SUM>(tree, vec16, p, threads)
-               : op == OP_MAX ? fused_occ_op<DT_BF16, OP_MAX>(tree, vec16, p, threads)
-               : op == OP_AVG ? fused_occ_op<DT_BF16, OP_AVG>(tree, vec16, p, threads)
-                              : fused_occ_op<DT_BF16, OP_AVG_PREDIV>(tree, vec16, p, threads);
-    default:
-        return op == OP_SUM ? fused_occ_op<DT_F16, OP_SUM>(tree, vec16, p, threads)
-               : op == OP_MAX ? fused_occ_op<DT_F16, OP_MAX>(tree, vec16, p, threads)
-               : op == OP_AVG ? fused_occ_op<DT_F16, OP_AVG>(tree, vec16, p, threads)
-                              : fused_occ_op<DT_F16, OP_AVG_PREDIV>(tree, vec16, p, threads);
-    }
 }
 
 }  // namespace rar

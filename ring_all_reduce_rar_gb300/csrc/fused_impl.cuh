@@ -398,11 +398,10 @@ static int sm_count_cached() {
 
 template <typename K>
 static cudaError_t launch_persistent(K kernel, const FusedArgs &a, long long work_items, int threads,
-                                     int grid_cap, cudaStream_t stream) {
+                                     cudaStream_t stream) {
     const int sms = sm_count_cached();
     const long long want = (work_items + threads - 1) / threads;
     long long grid = (long long)sms * blocks_per_sm_of(kernel, threads);
-    if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
     if (grid > want) grid = want;
     if (grid < 1) grid = 1;
     kernel<<<(unsigned)grid, threads, 0, stream>>>(a);
@@ -410,50 +409,28 @@ static cudaError_t launch_persistent(K kernel, const FusedArgs &a, long long wor
 }
 
 template <int DT, int OP, int P>
-static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int threads, int grid_cap,
-                                  cudaStream_t stream) {
+static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int threads, cudaStream_t stream) {
     constexpr int VE = 16 / ElemInfo<DT>::bytes;
     constexpr int U = (P > 0 && P <= 8) ? 2 : 1;
     if (tree) {
         if (vec16)
             return launch_persistent(fused_tree_order_kernel<DT, OP, P, true>, a, (a.n + VE - 1) / VE, threads,
-                                     grid_cap, stream);
-        return launch_persistent(fused_tree_order_kernel<DT, OP, P, false>, a, a.n, threads, grid_cap, stream);
+                                     stream);
+        return launch_persistent(fused_tree_order_kernel<DT, OP, P, false>, a, a.n, threads, stream);
     }
     if (vec16)
         return launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, a, ((a.n + VE - 1) / VE + U - 1) / U,
-                                 threads, grid_cap, stream);
-    return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, false>, a, a.n, threads, grid_cap, stream);
+                                 threads, stream);
+    return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, false>, a, a.n, threads, stream);
 }
 
 template <int DT, int OP>
-static cudaError_t launch_fused_op(const FusedArgs &a, bool tree, bool vec16, int threads, int grid_cap,
-                                   cudaStream_t stream) {
+static cudaError_t launch_fused_op(const FusedArgs &a, bool tree, bool vec16, int threads, cudaStream_t stream) {
     switch (a.p) {
-    case 4: return launch_fused_p<DT, OP, 4>(a, tree, vec16, threads, grid_cap, stream);
-    case 8: return launch_fused_p<DT, OP, 8>(a, tree, vec16, threads, grid_cap, stream);
-    case 16: return launch_fused_p<DT, OP, 16>(a, tree, vec16, threads, grid_cap, stream);
-    default: return launch_fused_p<DT, OP, 0>(a, tree, vec16, threads, grid_cap, stream);
-    }
-}
-
-template <int DT, int OP, int P>
-static int fused_occ_p(bool tree, bool vec16, int threads) {
-    constexpr int U = (P > 0 && P <= 8) ? 2 : 1;
-    if (tree)
-        return vec16 ? blocks_per_sm_of(fused_tree_order_kernel<DT, OP, P, true>, threads)
-                     : blocks_per_sm_of(fused_tree_order_kernel<DT, OP, P, false>, threads);
-    return vec16 ? blocks_per_sm_of(fused_ring_order_kernel<DT, OP, P, U, true>, threads)
-                 : blocks_per_sm_of(fused_ring_order_kernel<DT, OP, P, 1, false>, threads);
-}
-
-template <int DT, int OP>
-static int fused_occ_op(bool tree, bool vec16, int p, int threads) {
-    switch (p) {
-    case 4: return fused_occ_p<DT, OP, 4>(tree, vec16, threads);
-    case 8: return fused_occ_p<DT, OP, 8>(tree, vec16, threads);
-    case 16: return fused_occ_p<DT, OP, 16>(tree, vec16, threads);
-    default: return fused_occ_p<DT, OP, 0>(tree, vec16, threads);
+    case 4: return launch_fused_p<DT, OP, 4>(a, tree, vec16, threads, stream);
+    case 8: return launch_fused_p<DT, OP, 8>(a, tree, vec16, threads, stream);
+    case 16: return launch_fused_p<DT, OP, 16>(a, tree, vec16, threads, stream);
+    default: return launch_fused_p<DT, OP, 0>(a, tree, vec16, threads, stream);
     }
 }
 

@@ -379,7 +379,7 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
             return RAR_OK;
         }
         const int threads = 256;  // the fused kernels are compiled for 256 threads
-        cudaError_t ce = launch_fused(a, dtype, op, tree, vec16, threads, 0, stream);
+        cudaError_t ce = launch_fused(a, dtype, op, tree, vec16, threads, stream);
         if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the fused kernel");
         return RAR_OK;
     }

@@ -90,7 +90,7 @@ struct RingArgs {
 // Launchers (return cudaError_t of the launch).  `vec16` selects the 128-bit
 // path (all rank pointers 16-byte aligned).
 cudaError_t launch_fused(const FusedArgs &a, int dtype, int op, bool tree, bool vec16,
-                         int threads, int grid_cap, cudaStream_t stream);
+                         int threads, cudaStream_t stream);
 cudaError_t launch_ring(const RingArgs &a, int dtype, int op, bool vec16, int threads,
                         cudaStream_t stream);
 // Rank-sequential streaming fused path (PHASE_ALL, 16-byte aligned ranks);
@@ -107,7 +107,5 @@ cudaError_t launch_tree(const RingArgs &a, int dtype, int op, bool vec16, int th
 int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads);
 // Largest co-resident grid for the ring kernel of this dtype/op (per device).
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
-// Co-resident CTAs per SM for a fused kernel instance.
-int fused_blocks_per_sm(int dtype, int op, bool tree, bool vec16, int p, int threads);
 
 }  // namespace rar

@@ -59,7 +59,7 @@ def oracle_expect(host_rows, dtype, op, engine):
     ref = [w.to_storage_numpy(t).copy() for t in host_rows]
     if engine == "ring_bidir":
         sends = oracle.simulate_bidir(ref, dtype, op)
-    elif engine == "fused_tree":
+    elif engine in ("fused_tree", "tree"):
         oracle.tree_fold(ref, dtype, op)
         sends = None
     else:
@@ -86,10 +86,13 @@ def run_case(rar, dev, host_rows, dtype, op, engine, offset=0, **opts):
         got_sends = h.send_counts(len(rows))
     torch.cuda.synchronize()
     assert_bits_equal(rows, ref, f"{engine} {dtype} {op} p={len(rows)} n={rows[0].numel()}")
+    p, n = len(rows), rows[0].numel()
     if engine in ("ring", "ring_bidir"):
         assert list(got_sends) == list(sends)
+    elif engine == "tree":
+        assert sum(got_sends) == 2 * (p - 1) * n
     else:
-        assert list(got_sends) == [0] * len(rows)
+        assert list(got_sends) == [0] * p
 
 
 def gen(p, n, dtype, dist, seed):
@@ -282,6 +285,15 @@ def test_large_p_uses_pointer_table(rar, dev, engine):
     """p > 64: rank pointers travel through the device-side table."""
     p = 96 if engine == "fused" else 72
     host = gen(p, p * 50 + 7, "float32", ("normal", 1.0), 11)
+    run_case(rar, dev, host, "float32", "sum", engine)
+
+
+@pytest.mark.parametrize("engine", ["fused_regs", "fused_stream", "fused_tree", "tree"])
+def test_largest_p(rar, dev, engine):
+    """p at the top of the range: 1024 ranks (the fused engines: pointer
+    table, runtime p); 200 ranks for the tree executor (one CTA per rank)."""
+    p = 200 if engine == "tree" else 1024
+    host = gen(p, 2 * p + 37, "float32", ("normal", 1.0), 13)
     run_case(rar, dev, host, "float32", "sum", engine)
 
 

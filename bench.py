@@ -344,27 +344,58 @@ def run_sweep(args):
         _, rows = w.make_inputs(p, n, dtype, dist, w.seed_of(w.SWEEP_INDEX), device=dev)
         k = 200 if n <= 4 ** 9 else 20
         for eng in engines:
-            if eng == "tree" and op == "avg_prediv":
-                continue
-            with rar.Handle(0, engine=eng, skip_pointer_check=True) as h:
-                for _ in range(3):
-                    h.allreduce(rows, op=op)
-                h.check()
-                torch.cuda.synchronize()
-                torch.cuda._sleep(200_000_000)  # ~0.1 s of GPU time to queue behind
-                start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                start.record()
-                for _ in range(k):
-                    h.allreduce(rows, op=op)
-                end.record()
-                torch.cuda.synchronize()
-                assert h.status() == 0
-                us = start.elapsed_time(end) * 1e3 / k
+            us = device_us_per_call(rar, dict(engine=eng), rows, op, k)
             rb = (2 * p * n * e) if eng == "fused" else 5 * (p - 1) * n * e
             print(json.dumps({"sweep": f"p{p}_{dtype}_{op}", "engine": eng, "n": n, "us_per_call": round(us, 2),
                               "algbw_gbs": round(p * n * e / us / 1e3, 2),
                               "roofline_frac": round(rb / us / 1e3 / hbm_peak()[0], 4)}), flush=True)
         del rows
+        torch.cuda.empty_cache()
+
+
+def device_us_per_call(rar, opts, rows, op, k):
+    """Device time per call: the GPU is held by a short sleep kernel while
+    the host queues k calls, so events time back-to-back execution only."""
+    with rar.Handle(0, skip_pointer_check=True, **opts) as h:
+        for _ in range(3):
+            h.allreduce(rows, op=op)
+        h.check()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000_000)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(k):
+            h.allreduce(rows, op=op)
+        end.record()
+        torch.cuda.synchronize()
+        if h.status() != 0:
+            raise RuntimeError(rar.rar_last_error(h.h))
+        return start.elapsed_time(end) * 1e3 / k
+
+
+def run_configs(args):
+    """Every workload (p = 4 ... 64) on every engine: device time per call and
+    the fraction of the engine's HBM roofline; one JSON line each."""
+    import ring_all_reduce_rar_gb300 as rar
+    rar.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak = hbm_peak()[0]
+    engines = [("fused", dict(engine="fused")), ("ring", dict(engine="ring")),
+               ("ring_bidir", dict(engine="ring_bidir")), ("tree", dict(engine="tree"))]
+    for name, cfg in w.WORKLOADS.items():
+        p, n, dtype = cfg["p"], cfg["n"], cfg["dtype"]
+        e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
+        big, rows = w.make_inputs(p, n, dtype, cfg["dist"], w.seed_of(cfg["index"]), device=dev)
+        for op in cfg["ops"]:
+            for eng, opts in engines:
+                k = 10 if p * n * e > 1e9 else (50 if p * n * e > 1e7 else 200)
+                us = device_us_per_call(rar, opts, rows, op, k)
+                rb = 2 * p * n * e if eng == "fused" else 5 * (p - 1) * n * e
+                print(json.dumps({"workload": name, "op": op, "engine": eng, "us_per_call": round(us, 2),
+                                  "algbw_gbs": round(p * n * e / us / 1e3, 2),
+                                  "roofline_frac": round(rb / us / 1e3 / peak, 4)}), flush=True)
+        del big, rows
         torch.cuda.empty_cache()
 
 
@@ -416,6 +447,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="device time per call over the p = 16 message-size sweep (not the benchmark line)")
     ap.add_argument("--pair", type=int, default=0, help="--sweep: dtype/op pair of the sweep workload (0..2)")
+    ap.add_argument("--configs", action="store_true",
+                    help="device time per call of every workload on every engine (not the benchmark line)")
     ap.add_argument("--workload", choices=sorted(w.WORKLOADS), default="p8_n1073741824_bf16")
     ap.add_argument("--op", choices=["sum", "avg", "max"], default=None)
     ap.add_argument("--n", type=int, default=None,
@@ -426,6 +459,8 @@ def main():
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.sweep:
         run_sweep(args)
+    elif args.configs:
+        run_configs(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

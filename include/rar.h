@@ -57,6 +57,10 @@
  *     legacy default stream) and the call returns without waiting.  One call
  *     in flight per handle: calls on one stream are ordered; calls on several
  *     streams with one handle must be ordered by the caller.
+ *   - CUDA graphs: rar_allreduce, rar_reduce_scatter and rar_all_gather may
+ *     be recorded with stream capture and replayed any number of times; the
+ *     ring and tree executors keep their epoch in device memory, so every
+ *     replay is a fresh launch.  Create the handle outside the capture.
  *   - Trivial calls: p == 1 or n == 0 return RAR_OK and launch nothing (the
  *     torch ring in "An implementation" returns its tensor when p == 1);
  *     with n == 0 the rank pointers may be NULL.
@@ -211,10 +215,11 @@ int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bu
  * rar_last_error(NULL). */
 int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dtype, int op, void *stream);
 
-/* Synchronise the stream of the last call and return its device-side
- * status: RAR_OK, RAR_ETIMEOUT (a wait ran out; rar_last_error names the
- * rank and step), or RAR_EABORTED.  A timed-out call leaves the buffers
- * partly updated; the handle stays usable. */
+/* Synchronise the stream of the last call and return the device-side status:
+ * RAR_OK, or RAR_ETIMEOUT if a bounded wait ran out since the previous report
+ * (in the last call, or in a replay of a captured one); rar_last_error names
+ * the rank, step and slice.  Each failure is reported once.  A timed-out call
+ * leaves the buffers partly updated; the handle stays usable. */
 int rar_status(rar_handle h);
 
 /* Per-rank count of elements each rank sent in the last ring-engine call

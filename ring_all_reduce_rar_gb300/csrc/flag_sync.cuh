@@ -42,11 +42,12 @@ __device__ __forceinline__ int mod_p(int v, int p) {
     return v < 0 ? v + p : v;
 }
 
-// Record a timeout (first CTA of this call only) and raise the abort word.
-static __device__ void ring_give_up(const RingArgs &a, int rank, int step, long long slice, int nb,
-                             unsigned long long seen, unsigned long long wanted) {
-    unsigned prev = atomicMax(&a.status->epoch, a.epoch);
-    if (prev < a.epoch) {
+// Record a timeout and raise the abort word.  The first CTA of the launch
+// to give up fills in the details; every give-up bumps the sequence number.
+static __device__ void ring_give_up(const RingArgs &a, unsigned epoch, int rank, int step, long long slice, int nb,
+                                    unsigned long long seen, unsigned long long wanted) {
+    unsigned prev = atomicMax(&a.status->epoch, epoch);
+    if (prev < epoch) {
         a.status->code = RAR_ETIMEOUT;
         a.status->rank = rank;
         a.status->step = step;
@@ -56,13 +57,14 @@ static __device__ void ring_give_up(const RingArgs &a, int rank, int step, long 
         a.status->flag_wanted = wanted;
         __threadfence();
     }
-    atomicMax(a.abort_word, a.epoch);
+    atomicAdd(&a.status->seq, 1u);
+    atomicMax(a.abort_word, epoch);
 }
 
 // Bounded acquire-wait for the neighbour's progress word.  Returns false if
-// the wait ran out or another CTA aborted the call.
-static __device__ bool ring_wait(const RingArgs &a, const unsigned long long *flag, unsigned long long target, int rank,
-                          int step, long long slice, int nb) {
+// the wait ran out or another CTA aborted the launch.
+static __device__ bool ring_wait(const RingArgs &a, unsigned epoch, const unsigned long long *flag,
+                                 unsigned long long target, int rank, int step, long long slice, int nb) {
     unsigned long long v = ld_acquire_u64(flag);
     if (v >= target) return true;
     const unsigned long long t0 = global_ns();
@@ -71,11 +73,43 @@ static __device__ bool ring_wait(const RingArgs &a, const unsigned long long *fl
         __nanosleep(32);
         v = ld_acquire_u64(flag);
         if (v >= target) return true;
-        if (ld_relaxed_u32(a.abort_word) == a.epoch) return false;
+        if (ld_relaxed_u32(a.abort_word) == epoch) return false;
         if (it >= max_iters || global_ns() - t0 > a.timeout_ns) {
-            ring_give_up(a, rank, step, slice, nb, v, target);
+            ring_give_up(a, epoch, rank, step, slice, nb, v, target);
             return false;
         }
+    }
+}
+
+// The epoch of this launch: one more than the last finished launch's.  All
+// CTAs read the same value (the word only changes once every CTA finished).
+__device__ __forceinline__ unsigned launch_epoch_begin(const RingArgs &a) {
+    __shared__ unsigned s_epoch;
+    if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(a.epoch_word) + 1u;
+    __syncthreads();
+    return s_epoch;
+}
+
+// Every CTA calls this once, on every exit path, with all its threads.  The
+// last CTA to finish publishes the epoch for the next launch; on wrap-around
+// it first clears every progress word.
+__device__ __forceinline__ void launch_epoch_end(const RingArgs &a, unsigned epoch) {
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.finish_count, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    if (epoch == 0xFFFFFFFFu) {
+        for (int i = threadIdx.x; i < a.flag_capacity; i += blockDim.x) a.flags[i] = 0ull;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        *a.finish_count = 0u;
+        *a.epoch_word = epoch == 0xFFFFFFFFu ? 0u : epoch;
+        __threadfence();
     }
 }
 

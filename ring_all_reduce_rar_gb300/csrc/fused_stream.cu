@@ -294,17 +294,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     if (failed || *(volatile int *)&s_fail) {
         if (ct == 0) {
-            unsigned prev = atomicMax(&a.status->epoch, a.epoch);
-            if (prev < a.epoch) {
-                a.status->code = RAR_ETIMEOUT;
-                a.status->rank = -1;
-                a.status->step = -1;
-                a.status->slice = (int)(blockIdx.x + k * gridDim.x);
-                a.status->waited_on = -1;
-                a.status->flag_seen = 0;
-                a.status->flag_wanted = 0;
-                __threadfence();
-            }
+            a.status->code = RAR_ETIMEOUT;
+            a.status->rank = -1;
+            a.status->step = -1;
+            a.status->slice = (int)(blockIdx.x + k * gridDim.x);
+            a.status->waited_on = -1;
+            a.status->flag_seen = 0;
+            a.status->flag_wanted = 0;
+            __threadfence();
+            atomicAdd(&a.status->seq, 1u);
             st_bulk_commit();  // stores issued but not yet committed join a group
             st_bulk_wait_all();
         }

@@ -22,9 +22,10 @@
 // Set-up: the first call on a device (with that device current) takes the
 // array's device address with cudaGetSymbolAddress and clears the array
 // once; make that first call before any stream capture.
-// Every call shares the array: progress words carry the call's epoch, so no
-// per-call clearing is needed, but two calls that overlap on the GPU (on two
-// streams, or from two threads) race on the same words.  Order them.
+// Every call shares the array: progress words carry the launch's epoch (kept
+// in the array itself), so no per-call clearing is needed, but two calls
+// that overlap on the GPU (on two streams, or from two threads) race on the
+// same words.  Order them.
 #include <mutex>
 #include <string>
 
@@ -50,6 +51,8 @@ struct NoAllocScratch {
     unsigned long long recv_counts[kNoAllocMaxCtas];
     RingStatus status;
     unsigned abort_word;
+    unsigned epoch_word;    // the last finished launch's epoch
+    unsigned finish_count;  // CTAs of the running launch that finished
 };
 constexpr size_t kScratchWords = (sizeof(NoAllocScratch) + 7) / 8;
 
@@ -58,7 +61,6 @@ static __device__ __align__(256) unsigned long long g_noalloc_scratch[kScratchWo
 struct DeviceSlot {
     bool ready = false;
     NoAllocScratch *scratch = nullptr;  // device address of g_noalloc_scratch
-    unsigned epoch = 0;
 };
 
 std::mutex g_mutex;
@@ -118,7 +120,6 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     if (G < 1) return reject(RAR_EUNSUPPORTED, "p rank groups cannot be co-resident");
 
     NoAllocScratch *scratch = nullptr;
-    unsigned epoch = 0;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         DeviceSlot &slot = g_slots[dev];
@@ -132,18 +133,9 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
             if (ce != cudaSuccess)
                 return reject(RAR_ECUDA, std::string("clearing the scratch array: ") + cudaGetErrorString(ce));
             slot.scratch = static_cast<NoAllocScratch *>(addr);
-            slot.epoch = 0;
             slot.ready = true;
         }
-        if (++slot.epoch == 0) {
-            // epochs wrapped: clear the progress words once, in stream order
-            ce = cudaMemsetAsync(slot.scratch->flags, 0, sizeof(slot.scratch->flags), (cudaStream_t)stream);
-            if (ce != cudaSuccess)
-                return reject(RAR_ECUDA, std::string("clearing the progress words: ") + cudaGetErrorString(ce));
-            slot.epoch = 1;
-        }
         scratch = slot.scratch;
-        epoch = slot.epoch;
     }
 
     // slices: at most 64K elements, and few enough per channel and step to fit
@@ -166,7 +158,9 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.first_step = 0;
     a.n_steps = 2 * (p - 1);
     a.inv_p = 1.0f / (float)p;
-    a.epoch = epoch;
+    a.epoch_word = &scratch->epoch_word;
+    a.finish_count = &scratch->finish_count;
+    a.flag_capacity = kNoAllocMaxCtas;
     a.flags = scratch->flags;
     a.recv_counts = scratch->recv_counts;
     a.status = &scratch->status;

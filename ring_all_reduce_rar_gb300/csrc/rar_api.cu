@@ -33,16 +33,13 @@ struct rar_ctx {
     unsigned long long *recv_counts = nullptr;
     RingStatus *status = nullptr;
     unsigned *abort_word = nullptr;
+    unsigned *epoch_words = nullptr;  // [0] last finished launch's epoch, [1] finish counter
     void **ptr_table = nullptr;
-    unsigned epoch = 0;
+    unsigned acked_seq = 0;           // status failures already reported
     // last call, for rar_status / rar_send_counts
     bool have_last = false;
     cudaStream_t last_stream = nullptr;
     bool last_ring = false;
-    // epochs of the last call's launches that can record a status: [lo, hi]
-    // (0, 0 when none can)
-    unsigned last_status_lo = 0;
-    unsigned last_status_hi = 0;
     int last_p = 0;
     // ring launches of the last call (the hierarchical schedule makes three)
     int last_phases = 0;
@@ -148,17 +145,6 @@ int fill_ptrs(rar_ctx *h, RankPtrs &rp, void *const *bufs, int p, cudaStream_t s
     return RAR_OK;
 }
 
-// Next call epoch (never 0).  When the counter wraps, the progress words are
-// cleared once in stream order so that no stale word can satisfy a wait.
-int next_epoch(rar_ctx *h, cudaStream_t stream) {
-    if (++h->epoch == 0) {
-        cudaError_t ce = cudaMemsetAsync(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas, stream);
-        if (ce != cudaSuccess) return cuda_fail(h, ce, "resetting the progress words");
-        h->epoch = 1;
-    }
-    return RAR_OK;
-}
-
 bool all_aligned16(void *const *bufs, int p) {
     for (int r = 0; r < p; r++)
         if ((uintptr_t)bufs[r] % 16) return false;
@@ -204,8 +190,6 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dty
     slice = std::max<long long>(16, (slice + 15) / 16 * 16);
     while ((maxchunk + slice - 1) / slice / min_g > kMaxSlicesPerChannelStep) slice *= 2;
 
-    int rc = next_epoch(h, stream);
-    if (rc != RAR_OK) return rc;
     RingArgs a;
     a.bufs = ptrs;
     a.n = (long long)n;
@@ -219,7 +203,9 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dty
     a.first_step = first;
     a.n_steps = steps;
     a.inv_p = 1.0f / (float)p;
-    a.epoch = h->epoch;
+    a.epoch_word = h->epoch_words;
+    a.finish_count = h->epoch_words + 1;
+    a.flag_capacity = kMaxRingCtas;
     a.flags = h->flags;
     a.recv_counts = h->recv_counts + (size_t)phase_idx * kMaxRingCtas;
     a.status = h->status;
@@ -234,8 +220,6 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dty
         return cuda_fail(h, ce, "launching the ring executor");
     }
     h->last_ring = true;
-    if (h->last_status_lo == 0) h->last_status_lo = h->epoch;
-    h->last_status_hi = h->epoch;
     h->last_layout[phase_idx] = layout;
     h->last_channels[phase_idx] = G;
     h->last_fwd_channels[phase_idx] = fwd_channels;
@@ -263,8 +247,6 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     }
     slice = std::max<long long>(16, (slice + 15) / 16 * 16);
     while (((long long)n + slice - 1) / slice / G > kMaxSlicesPerChannelStep - 1) slice *= 2;
-    int rc = next_epoch(h, stream);
-    if (rc != RAR_OK) return rc;
     cudaError_t ce = cudaMemsetAsync(h->recv_counts, 0, sizeof(unsigned long long) * (size_t)p, stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the send counters");
     RingArgs a;
@@ -280,7 +262,9 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     a.first_step = 0;
     a.n_steps = 0;
     a.inv_p = 1.0f / (float)p;
-    a.epoch = h->epoch;
+    a.epoch_word = h->epoch_words;
+    a.finish_count = h->epoch_words + 1;
+    a.flag_capacity = kMaxRingCtas;
     a.flags = h->flags;
     a.recv_counts = h->recv_counts;
     a.status = h->status;
@@ -295,7 +279,6 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
         return cuda_fail(h, ce, "launching the tree executor");
     }
     h->last_ring = true;
-    h->last_status_lo = h->last_status_hi = h->epoch;
     h->last_layout[0] = TREE;
     h->last_channels[0] = G;
     h->last_fwd_channels[0] = G;
@@ -314,7 +297,6 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     h->have_last = true;
     h->last_stream = stream;
     h->last_ring = false;
-    h->last_status_lo = h->last_status_hi = 0;
     h->last_phases = 0;
     h->last_p = p;
     if (n == 0 || p == 1) return RAR_OK;
@@ -338,7 +320,6 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         a.phase = phase;
         a.inv_p = inv_p;
         a.status = h->status;
-        a.epoch = 0;
         a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
         const bool tree = engine == RAR_ENGINE_FUSED_TREE && phase != PHASE_AG;
         if (hier) {
@@ -361,9 +342,6 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
                         "the streaming path needs engine fused, a full all-reduce and 16-byte aligned rank buffers");
         if (path == 0) path = (stream_ok && (p > 16 || bytes >= (size_t)80 << 20)) ? 2 : 1;
         if (path == 2) {
-            rc = next_epoch(h, stream);
-            if (rc != RAR_OK) return rc;
-            a.epoch = h->epoch;
             // tile per rank (slice_elems, else 32 KB, halved while there are
             // fewer than four tiles per SM); stages (channels, else 3)
             size_t tb = h->opt.slice_elems ? (size_t)h->opt.slice_elems * (size_t)elem_bytes(dtype) : 32768;
@@ -375,7 +353,6 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
                 return fail(h, RAR_EINVAL, "streaming path: stages (channels) must be in [2, 8] and fit in 227 KB");
             cudaError_t ce = launch_fused_stream(a, dtype, op, (int)tb, stages, stream);
             if (ce != cudaSuccess) return cuda_fail(h, ce, "launching the streaming fused kernel");
-            h->last_status_lo = h->last_status_hi = h->epoch;
             return RAR_OK;
         }
         const int threads = 256;  // the fused kernels are compiled for 256 threads
@@ -458,12 +435,14 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
               cudaMalloc((void **)&h->recv_counts, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
               cudaMalloc((void **)&h->status, sizeof(RingStatus)) == cudaSuccess &&
               cudaMalloc((void **)&h->abort_word, sizeof(unsigned)) == cudaSuccess &&
+              cudaMalloc((void **)&h->epoch_words, 2 * sizeof(unsigned)) == cudaSuccess &&
               cudaMalloc((void **)&h->ptr_table, sizeof(void *) * RAR_MAX_P) == cudaSuccess;
     if (ok) {
         ok = cudaMemset(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
              cudaMemset(h->recv_counts, 0, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
              cudaMemset(h->status, 0, sizeof(RingStatus)) == cudaSuccess &&
              cudaMemset(h->abort_word, 0, sizeof(unsigned)) == cudaSuccess &&
+             cudaMemset(h->epoch_words, 0, 2 * sizeof(unsigned)) == cudaSuccess &&
              cudaDeviceSynchronize() == cudaSuccess;
     }
     if (!ok) {
@@ -472,6 +451,7 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
         cudaFree(h->recv_counts);
         cudaFree(h->status);
         cudaFree(h->abort_word);
+        cudaFree(h->epoch_words);
         cudaFree(h->ptr_table);
         delete h;
         return fail(nullptr, RAR_ENOMEM, "allocating the handle's scratch failed");
@@ -555,11 +535,13 @@ int rar_status(rar_handle h) {
     DeviceGuard dg(h->device);
     cudaError_t ce = cudaStreamSynchronize(h->last_stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "synchronising the last call's stream");
-    if (h->last_status_lo == 0) return RAR_OK;
     RingStatus st{};
     ce = cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the status word");
-    if (st.epoch >= h->last_status_lo && st.epoch <= h->last_status_hi && st.code != 0) {
+    if (st.seq != h->acked_seq) {
+        // a wait ran out since the last report (this call, or a replay of a
+        // captured one)
+        h->acked_seq = st.seq;
         char buf[256];
         if (st.rank >= 0)
             std::snprintf(buf, sizeof(buf),
@@ -569,7 +551,7 @@ int rar_status(rar_handle h) {
         else
             std::snprintf(buf, sizeof(buf), "bulk-copy wait timed out on tile %d", st.slice);
         h->err = buf;
-        return (int)st.code;
+        return st.code ? (int)st.code : RAR_ETIMEOUT;
     }
     return RAR_OK;
 }
@@ -631,6 +613,7 @@ int rar_destroy(rar_handle h) {
         cudaFree(h->recv_counts);
         cudaFree(h->status);
         cudaFree(h->abort_word);
+        cudaFree(h->epoch_words);
         cudaFree(h->ptr_table);
     }
     delete h;

@@ -26,9 +26,11 @@ struct RankPtrs {
     void *const *table;  // device array of p pointers when p > kInlineP
 };
 
-// Device-side status of a launch (written by the first CTA that gives up).
+// Device-side status: a CTA whose bounded wait runs out fills in the
+// details and bumps `seq`; the host reports a failure when `seq` moved.
 struct RingStatus {
-    unsigned epoch;   // epoch of the call that failed (0: none yet)
+    unsigned epoch;   // ring/tree: the epoch of the launch that failed (first reporter of a launch)
+    unsigned seq;     // number of give-ups so far (never reset)
     unsigned code;    // RAR_ETIMEOUT
     int rank;         // rank whose wait ran out
     int step;         // global schedule step it was waiting to start
@@ -47,7 +49,6 @@ struct FusedArgs {
     float inv_p;   // binary32 nearest to 1/p
     // streaming path only: where a bounded wait that ran out is recorded
     RingStatus *status;
-    unsigned epoch;
     unsigned long long timeout_ns;
 };
 
@@ -76,11 +77,16 @@ struct RingArgs {
     int first_step;      // global schedule steps [first_step, first_step + n_steps)
     int n_steps;
     float inv_p;
-    unsigned epoch;
+    // Device-side epochs: a launch uses *epoch_word + 1; the last CTA to
+    // finish (counted in *finish_count) stores it back, so every launch --
+    // also every replay of a captured one -- gets a fresh epoch.
+    unsigned *epoch_word;
+    unsigned *finish_count;
+    int flag_capacity;                // progress words to clear when the epoch wraps
     unsigned long long *flags;        // [p * channels] progress words
     unsigned long long *recv_counts;  // [p * channels] elements received by each CTA
     RingStatus *status;
-    unsigned *abort_word;             // == epoch once any CTA gave up
+    unsigned *abort_word;             // == the launch's epoch once any CTA gave up
     unsigned long long timeout_ns;
     int fault_mode;
     int fault_rank;

@@ -16,8 +16,9 @@
 // slice with a release store of a 64-bit word
 //     (epoch << 32) | (step << 20) | (slice-within-channel + 1),
 // and the right neighbour's CTA of the same channel acquires it before it
-// reads that slice at the next step.  Epoch-tagged words need no reset
-// between calls.
+// reads that slice at the next step.  The epoch comes from device memory
+// (flag_sync.cuh), so the words need no reset between launches and a launch
+// captured in a CUDA graph can be replayed.
 //
 // In-place safety: rank r - 1 overwrites the chunk r read at reduce-scatter
 // step s only at its all-gather step s, and that write waits on a chain of
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
         seg_lo = chunk_start(c, gb, ge);
         L = gb + (c < ge ? 1 : 0);
     }
+    const unsigned epoch = launch_epoch_begin(a);
     const int nb_pos = fwd ? mod_p(pos - 1, rp) : mod_p(pos + 1, rp);
     const int nb = ring_base + nb_pos * ring_step;  // the rank this CTA receives from
     // avg scales once, at the final owner; pre-division scales each original
@@ -165,9 +167,9 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
                 if (threadIdx.x == 0) {
                     bool ok;
                     if (step > a.first_step)
-                        ok = ring_wait(a, nb_flag, progress_tag(a.epoch, step - 1, loc), r, step, sl, nb);
+                        ok = ring_wait(a, epoch, nb_flag, progress_tag(epoch, step - 1, loc), r, step, sl, nb);
                     else
-                        ok = ld_relaxed_u32(a.abort_word) != a.epoch;
+                        ok = ld_relaxed_u32(a.abort_word) != epoch;
                     if (ok && slow) ring_delay(a.fault_delay_ns);
                     s_stop = ok ? 0 : 1;
                 }
@@ -183,13 +185,14 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
                 __syncthreads();
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    st_release_u64(my_flag, progress_tag(a.epoch, step, loc));
+                    st_release_u64(my_flag, progress_tag(epoch, step, loc));
                 }
             }
         }
     }
 done:
     if (threadIdx.x == 0) a.recv_counts[blockIdx.x] = received;
+    launch_epoch_end(a, epoch);
 }
 
 template <int DT, int OP, bool VEC>

@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __
     const long long nsl = (a.n + a.slice - 1) / a.slice;
     const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
     const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
-    if (muted) return;
+    const unsigned epoch = launch_epoch_begin(a);
+    if (muted) goto done;
 
     for (int t = 0; t < 2 * L; t++) {
         const bool up = t < L;
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __
             // nothing to do: the step is passed as soon as the previous one is
             if (threadIdx.x == 0) {
                 __threadfence();
-                st_release_u64(my_flag, progress_tag(a.epoch, t, kTreePassLoc));
+                st_release_u64(my_flag, progress_tag(epoch, t, kTreePassLoc));
             }
             continue;
         }
@@ -98,13 +99,13 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __
         for (long long sl = j; sl < nsl; sl += a.channels, loc++) {
             if (threadIdx.x == 0) {
                 // the peer's data is final for this slice once it passed step t - 1
-                bool ok = t > 0 ? ring_wait(a, peer_flag, progress_tag(a.epoch, t - 1, loc), r, t, sl, peer)
-                                : ld_relaxed_u32(a.abort_word) != a.epoch;
+                bool ok = t > 0 ? ring_wait(a, epoch, peer_flag, progress_tag(epoch, t - 1, loc), r, t, sl, peer)
+                                : ld_relaxed_u32(a.abort_word) != epoch;
                 if (ok && slow) ring_delay(a.fault_delay_ns);
                 s_stop = ok ? 0 : 1;
             }
             __syncthreads();
-            if (s_stop) return;
+            if (s_stop) goto done;
             const long long lo = sl * a.slice;
             const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
             tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, root_last, a.inv_p);
@@ -112,10 +113,12 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __
             if (threadIdx.x == 0) {
                 atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // elements the peer sent
                 __threadfence();
-                st_release_u64(my_flag, progress_tag(a.epoch, t, loc));
+                st_release_u64(my_flag, progress_tag(epoch, t, loc));
             }
         }
     }
+done:
+    launch_epoch_end(a, epoch);
 }
 
 template <int DT, int OP, bool VEC>

@@ -549,6 +549,39 @@ def test_tree_executor_fault_and_rejections(rar, dev):
         assert e.value.code == 2
 
 
+# ----------------------------------------------------------------- CUDA graphs
+
+@pytest.mark.parametrize("engine,opts", [("fused_regs", {}), ("fused_stream", {}), ("ring", {}),
+                                         ("ring_bidir", {}), ("tree", {}), ("ring", dict(hier_group=2)),
+                                         ("fused_tree", {})])
+def test_captured_call_replays(rar, dev, engine, opts):
+    """A call recorded with stream capture replays correctly again and again:
+    the ring and tree executors take their epoch from device memory."""
+    p, n = 8, 8 * 3000 + 5
+    host = gen(p, n, "bfloat16", ("normal", 1e-2), 60)
+    if opts.get("hier_group"):
+        ref = [w.to_storage_numpy(t).copy() for t in host]
+        oracle.hier_simulate(ref, opts["hier_group"], "bfloat16", "sum")
+    else:
+        ref, _ = oracle_expect(host, "bfloat16", "sum", engine)
+    big, rows = upload(host, dev)
+    with rar.Handle(0, **handle_opts(engine, **opts)) as h:
+        graph = torch.cuda.CUDAGraph()
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                h.allreduce(rows, stream=stream)
+        torch.cuda.synchronize()
+        for replay in range(3):
+            for r in range(p):
+                rows[r].copy_(host[r])
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert h.status() == 0
+            assert_bits_equal(rows, ref, f"{engine} {opts} replay {replay}")
+
+
 # ----------------------------------------------------------------- host buffers
 
 @pytest.mark.parametrize("engine", ["fused", "fused_stream", "ring"])

@@ -69,14 +69,18 @@ static __device__ bool ring_wait(const RingArgs &a, unsigned epoch, const unsign
     if (v >= target) return true;
     const unsigned long long t0 = global_ns();
     const unsigned long long max_iters = a.timeout_ns / 16ull + (1ull << 20);
+    // spin on the word first (a hand-off usually lands within a few polls),
+    // then back off; the abort word and the clock are read every 16th poll
     for (unsigned long long it = 0;; it++) {
-        __nanosleep(32);
+        if (it >= 64) __nanosleep(64);
         v = ld_acquire_u64(flag);
         if (v >= target) return true;
-        if (ld_relaxed_u32(a.abort_word) == epoch) return false;
-        if (it >= max_iters || global_ns() - t0 > a.timeout_ns) {
-            ring_give_up(a, epoch, rank, step, slice, nb, v, target);
-            return false;
+        if ((it & 15) == 15) {
+            if (ld_relaxed_u32(a.abort_word) == epoch) return false;
+            if (it >= max_iters || global_ns() - t0 > a.timeout_ns) {
+                ring_give_up(a, epoch, rank, step, slice, nb, v, target);
+                return false;
+            }
         }
     }
 }

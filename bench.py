@@ -57,12 +57,20 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources, to tell whether stored ncu counters still
-    describe the kernels being timed."""
+# The sources that make each timed kernel and its launch configuration.
+ENGINE_SOURCES = {
+    "fused": ("rar_internal.h", "elem_ops.cuh", "fused_impl.cuh", "fused.cu", "fused_stream.cu", "rar_api.cu"),
+    "ring": ("rar_internal.h", "elem_ops.cuh", "flag_sync.cuh", "ring.cu", "rar_api.cu"),
+}
+ENGINE_SOURCES["ring_bidir"] = ENGINE_SOURCES["ring"]
+
+
+def kernel_source_hash(engine: str) -> str:
+    """Hash of the CUDA sources behind one engine's kernel, to tell whether
+    stored ncu counters still describe the kernel being timed."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ring_all_reduce_rar_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ENGINE_SOURCES[engine]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -78,7 +86,7 @@ def stored_traffic(engine: str, workload: str):
     except Exception:
         return None
     ent = d.get(workload, {}).get(engine)
-    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+    if not ent or engine not in ENGINE_SOURCES or ent.get("kernel_source_hash") != kernel_source_hash(engine):
         return None
     return ent.get("dram_bytes_per_launch")
 

@@ -175,6 +175,22 @@ int rar_reduce_scatter(rar_handle h, void *const *bufs, int p, size_t n, int dty
  * Same arguments and errors as rar_allreduce (op is not taken). */
 int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, void *stream);
 
+/* In-place all-reduce of the index range [lo, hi) of p rank buffers of
+ * n_total elements each: bufs[r] points at element lo of rank r's buffer
+ * (hi - lo elements behind it, owned by the caller).  Chunks are cut from
+ * n_total by chunk_bounds, and every element is reduced in its chunk's order,
+ * so the range ends up exactly as rar_allreduce over the whole buffers leaves
+ * it, bit for bit, with the handle's engine.  The pages have no such call;
+ * it rests on each result element depending only on the inputs at its index
+ * and on its chunk: disjoint ranges can be reduced by separate calls (on
+ * separate streams, or on the GPUs that hold them) without any exchange.
+ * Send counts (rar_send_counts) are the elements moved for this range; over
+ * ranges that cover [0, n_total) they add up to the whole call's counts.
+ * Errors: as rar_allreduce; RAR_EINVAL unless lo <= hi <= n_total.
+ * lo == hi is a no-op. */
+int rar_allreduce_range(rar_handle h, void *const *bufs, int p, size_t n_total, size_t lo, size_t hi, int dtype,
+                        int op, void *stream);
+
 /* All-reduce of host-resident rank buffers, with the handle's engine.
  *   host_bufs  host array of p host pointers, n elements each; the result
  *              replaces the inputs

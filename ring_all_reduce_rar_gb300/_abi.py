@@ -91,6 +91,7 @@ def load_library():
         for name in ("rar_allreduce", "rar_reduce_scatter"):
             getattr(lib, name).argtypes = [vp, ctypes.POINTER(vp), i32, sz, i32, i32, vp]
         lib.rar_all_gather.argtypes = [vp, ctypes.POINTER(vp), i32, sz, i32, vp]
+        lib.rar_allreduce_range.argtypes = [vp, ctypes.POINTER(vp), i32, sz, sz, sz, i32, i32, vp]
         lib.rar_allreduce_host.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, sz, i32, i32, vp]
         lib.rar_allreduce_noalloc.argtypes = [ctypes.POINTER(vp), i32, sz, i32, i32, vp]
         lib.rar_status.argtypes = [vp]
@@ -100,7 +101,7 @@ def load_library():
         lib.rar_destroy.argtypes = [vp]
         lib.rar_version.argtypes = []
         for name in ("rar_init", "rar_set_options", "rar_allreduce", "rar_reduce_scatter",
-                     "rar_all_gather", "rar_allreduce_host", "rar_allreduce_noalloc", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
+                     "rar_all_gather", "rar_allreduce_range", "rar_allreduce_host", "rar_allreduce_noalloc", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -174,6 +175,15 @@ def rar_reduce_scatter(handle: int, tensors, op: str = "sum", stream=None) -> No
 def rar_all_gather(handle: int, tensors, stream=None) -> None:
     arr, p, n, dt, dev = _marshal(tensors)
     _check(handle, load_library().rar_all_gather(handle, arr, p, n, dt, _stream_ptr(stream, dev)))
+
+
+def rar_allreduce_range(handle: int, tensors, n_total: int, lo: int, op: str = "sum", stream=None) -> None:
+    """All-reduce of indices [lo, lo + numel) of rank buffers of n_total
+    elements (see rar_allreduce_range in rar.h): `tensors` are the pieces,
+    element 0 of each being global index lo."""
+    arr, p, n, dt, dev = _marshal(tensors)
+    _check(handle, load_library().rar_allreduce_range(handle, arr, p, n_total, lo, lo + n, dt, OP_CODES[op],
+                                                        _stream_ptr(stream, dev)))
 
 
 def rar_allreduce_host(handle: int, host_tensors, dev_tensors=None, op: str = "sum", stream=None) -> None:
@@ -253,6 +263,9 @@ class Handle:
 
     def allreduce(self, tensors, op="sum", stream=None):
         rar_allreduce(self.h, tensors, op, stream)
+
+    def allreduce_range(self, tensors, n_total, lo, op="sum", stream=None):
+        rar_allreduce_range(self.h, tensors, n_total, lo, op, stream)
 
     def allreduce_host(self, host_tensors, dev_tensors=None, op="sum", stream=None):
         rar_allreduce_host(self.h, host_tensors, dev_tensors, op, stream)

@@ -133,16 +133,17 @@ template <int DT, int OP, int P, int U, bool VEC>
 __global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const __grid_constant__ FusedArgs a) {
     const int p = P > 0 ? P : a.p;
     const long long n = a.n;
-    const long long base = n / p, extra = n % p;
+    const long long base = a.n_total / p, extra = a.n_total % p;
+    const long long g0 = a.first;  // global index of local element 0
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;  // elements per vector
     const long long nvec = (n + VE - 1) / VE;
     const long long nfull = n / VE;
     const long long tv = (long long)blockDim.x * U;
     for (long long t0 = (long long)blockIdx.x * tv; t0 < nvec; t0 += (long long)gridDim.x * tv) {
         const long long t1 = t0 + tv < nvec ? t0 + tv : nvec;
-        const int c0 = chunk_of(t0 * VE, base, extra);
+        const int c0 = chunk_of(g0 + t0 * VE, base, extra);
         const long long last = (t1 * VE < n ? t1 * VE : n) - 1;
-        const int c1 = chunk_of(last, base, extra);
+        const int c1 = chunk_of(g0 + last, base, extra);
         if (VEC && t1 - t0 == tv && t1 <= nfull && c0 == c1) {
             fused_fold_vectors<DT, OP, P, U>(a, p, c0, t0 + threadIdx.x, blockDim.x);
             continue;
@@ -153,8 +154,8 @@ __global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const _
             if (v >= t1) break;
             const long long e0 = v * VE;
             if (VEC && v < nfull) {
-                const int ca = chunk_of(e0, base, extra);
-                const int cb = chunk_of(e0 + VE - 1, base, extra);
+                const int ca = chunk_of(g0 + e0, base, extra);
+                const int cb = chunk_of(g0 + e0 + VE - 1, base, extra);
                 if (ca == cb) {
                     fused_fold_vectors<DT, OP, P, 1>(a, p, ca, v, 0);
                     continue;
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const _
             for (int l = 0; l < VE; l++) {
                 const long long i = e0 + l;
                 if (i >= n) break;
-                fused_fold_element<DT, OP>(a, p, chunk_of(i, base, extra), i);
+                fused_fold_element<DT, OP>(a, p, chunk_of(g0 + i, base, extra), i);
             }
         }
     }
@@ -236,15 +237,16 @@ template <int DT, int OP, int P, bool VEC>
 __global__ void __launch_bounds__(kFusedThreads) fused_tree_order_kernel(const __grid_constant__ FusedArgs a) {
     const int p = P > 0 ? P : a.p;
     const long long n = a.n;
-    const long long base = n / p, extra = n % p;
+    const long long base = a.n_total / p, extra = a.n_total % p;
+    const long long g0 = a.first;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
     const long long nvec = (n + VE - 1) / VE;
     const long long nfull = n / VE;
     for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
          v += (long long)gridDim.x * blockDim.x) {
         const long long e0 = v * VE;
-        const int ca = chunk_of(e0, base, extra);
-        const int cb = chunk_of((e0 + VE - 1 < n ? e0 + VE - 1 : n - 1), base, extra);
+        const int ca = chunk_of(g0 + e0, base, extra);
+        const int cb = chunk_of(g0 + (e0 + VE - 1 < n ? e0 + VE - 1 : n - 1), base, extra);
         if (VEC && v < nfull && (a.phase == PHASE_ALL || ca == cb)) {
             uint4 acc = tree_fold_vector<DT, OP, P>(a, p, v);
             if constexpr (OP == OP_AVG) acc = scale_vec<DT>(acc, a.inv_p);
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_tree_order_kernel(const _
             uint32_t acc = tree_fold_element<DT, OP, P>(a, p, i);
             if constexpr (OP == OP_AVG) acc = scale_word<DT>(acc, a.inv_p);
             if (a.phase == PHASE_RS) {
-                const int c = chunk_of(i, base, extra);
+                const int c = chunk_of(g0 + i, base, extra);
                 store_elem<DT>(rank_ptr(a.bufs, p, (c == 0) ? p - 1 : c - 1), i, acc);
             } else {
                 for (int r = 0; r < p; r++) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
@@ -351,6 +353,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel(const __grid_
     const int p = a.p;
     const int m = p / g;
     const long long n = a.n;
+    const long long nt = a.n_total, g0 = a.first;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
     const long long nvec = (n + VE - 1) / VE;
     const long long nfull = n / VE;
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel(const __grid_
          v += (long long)gridDim.x * blockDim.x) {
         const long long e0 = v * VE;
         if (VEC && v < nfull) {
-            const HierPos a0 = hier_pos(e0, n, g, m), a1 = hier_pos(e0 + VE - 1, n, g, m);
+            const HierPos a0 = hier_pos(g0 + e0, nt, g, m), a1 = hier_pos(g0 + e0 + VE - 1, nt, g, m);
             if (a0.c == a1.c && a0.s == a1.s) {
                 const uint4 acc = hier_fold_vector<DT, OP>(a, p, g, a0, v);
                 for (int r = 0; r < p; r++) __stcs(reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, r)) + v, acc);
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel(const __grid_
         for (int l = 0; l < VE; l++) {
             const long long i = e0 + l;
             if (i >= n) break;
-            const uint32_t acc = hier_fold_element<DT, OP>(a, p, g, hier_pos(i, n, g, m), i);
+            const uint32_t acc = hier_fold_element<DT, OP>(a, p, g, hier_pos(g0 + i, nt, g, m), i);
             for (int r = 0; r < p; r++) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
         }
     }

@@ -106,7 +106,7 @@ __device__ __noinline__ void stream_straddling_vector(const FusedArgs &a, int p,
     constexpr int VE = 16 / EB;
     for (int l = 0; l < VE; l++) {
         const long long i = i0 + l;
-        const int c = chunk_of(i, base, extra);
+        const int c = chunk_of(a.first + i, base, extra);
         uint32_t acc = contrib_word<DT, OP>(load_elem<DT>(rank_ptr(a.bufs, p, c), i), a.inv_p);
         for (int k = 1; k < p; k++) {
             int r = c + k;
@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const long long n = a.n;
     const long long bulk_bytes = (n * EB) & ~15ll;
     const long long ntiles = (bulk_bytes + TB - 1) / TB;
-    const long long base = n / p, extra = n % p;
+    const long long base = a.n_total / p, extra = a.n_total % p;
+    const long long g0 = a.first;  // global index of local element 0
     unsigned char *stage = smem;                               // NS * TB
     unsigned char *result = smem + (size_t)NS * TB;            // 2 * TB
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)(NS + 2) * TB);
@@ -157,9 +158,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         const long long off = tile_off(k);
         return (uint32_t)(bulk_bytes - off < TB ? bulk_bytes - off : TB);
     };
-    auto tile_first_chunk = [&](long long k) { return chunk_of(tile_off(k) / EB, base, extra); };
+    auto tile_first_chunk = [&](long long k) { return chunk_of(g0 + tile_off(k) / EB, base, extra); };
     auto tile_segments = [&](long long k) {
-        const long long e0 = tile_off(k) / EB;
+        const long long e0 = g0 + tile_off(k) / EB;
         return chunk_of(e0 + tile_len(k) / EB - 1, base, extra) - chunk_of(e0, base, extra) + 1;
     };
 
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             seg[u] = 0;
             if (m > 1 && v < nvec) {
                 const long long i0 = e0 + (long long)v * VE;
-                const int ca = chunk_of(i0, base, extra), cb = chunk_of(i0 + VE - 1, base, extra);
+                const int ca = chunk_of(g0 + i0, base, extra), cb = chunk_of(g0 + i0 + VE - 1, base, extra);
                 seg[u] = ca == cb ? ca - c0 : -1;
             }
         }
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     if (ct == 0)
         while (pend_next < pend_count) issue_pending_store();
     if (blockIdx.x == gridDim.x - 1 && ct == 0) {
-        for (long long i = bulk_bytes / EB; i < n; i++) fused_fold_element<DT, OP>(a, p, chunk_of(i, base, extra), i);
+        for (long long i = bulk_bytes / EB; i < n; i++) fused_fold_element<DT, OP>(a, p, chunk_of(g0 + i, base, extra), i);
     }
     if (ct == 0) st_bulk_wait_all();
 }

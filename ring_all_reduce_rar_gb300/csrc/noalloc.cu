@@ -148,6 +148,8 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     for (int r = 0; r < kInlineP; r++) a.bufs.inl[r] = r < p ? bufs[r] : nullptr;
     a.bufs.table = nullptr;
     a.n = (long long)n;
+    a.first = 0;
+    a.n_total = (long long)n;
     a.p = p;
     a.layout = RING_FLAT;
     a.group = p;

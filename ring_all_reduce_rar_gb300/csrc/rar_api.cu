@@ -155,8 +155,9 @@ bool all_aligned16(void *const *bufs, int p) {
 // across nodes), steps [first, first + steps) of that ring size, counters in
 // array `phase_idx`.  Channels and slices follow the tuned defaults unless
 // the options set them.
-int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dtype, int op, bool vec16, bool bidir,
-                      int layout, int group, int first, int steps, int phase_idx, cudaStream_t stream) {
+int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long long g_first, long long n_total,
+                      int dtype, int op, bool vec16, bool bidir, int layout, int group, int first, int steps,
+                      int phase_idx, cudaStream_t stream) {
     const int threads = h->opt.block_threads ? h->opt.block_threads : 512;
     if (threads > 512) return fail(h, RAR_EINVAL, "ring engines run at most 512 threads per CTA");
     int per_sm = 0;
@@ -173,14 +174,13 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dty
         if (G < (bidir ? 2 : 1))
             return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
     }
-    const long long split = bidir ? (long long)n - (long long)n / 2 : (long long)n;  // chunk_bounds(n, 2)
+    const long long split = bidir ? n_total - n_total / 2 : n_total;  // chunk_bounds(n_total, 2)
     const int fwd_channels = bidir ? (G + 1) / 2 : G;
     const int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
-    // the longest chunk any ring of this launch moves
+    // the longest chunk piece any ring of this launch moves
     const int rp = layout == RING_FLAT ? p : layout == RING_INTRA ? group : p / group;
-    const long long seg = layout == RING_INTER ? ((long long)n + group - 1) / group
-                                               : std::max(split, (long long)n - split);
-    const long long maxchunk = (seg + rp - 1) / rp;
+    const long long seg = layout == RING_INTER ? (n_total + group - 1) / group : std::max(split, n_total - split);
+    const long long maxchunk = std::min((seg + rp - 1) / rp, (long long)n);
     long long slice = h->opt.slice_elems;
     if (slice == 0) {
         slice = (maxchunk + min_g - 1) / min_g;
@@ -193,6 +193,8 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dty
     RingArgs a;
     a.bufs = ptrs;
     a.n = (long long)n;
+    a.first = g_first;
+    a.n_total = n_total;
     a.p = p;
     a.layout = layout;
     a.group = group;
@@ -252,6 +254,8 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     RingArgs a;
     a.bufs = ptrs;
     a.n = (long long)n;
+    a.first = 0;  // the tree's order does not depend on the index
+    a.n_total = (long long)n;
     a.p = p;
     a.layout = TREE;
     a.group = p;
@@ -287,10 +291,14 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     return RAR_OK;
 }
 
+// n elements behind each pointer; they are global indices
+// [g_first, g_first + n) of rank buffers of n_total elements (g_first = 0,
+// n_total = n for a whole-buffer call).
 int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int phase, void *stream_v,
-        bool host_mapped = false) {
+        bool host_mapped = false, long long g_first = 0, long long n_total = -1) {
     if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
     h->err.clear();
+    if (n_total < 0) n_total = (long long)n;
     int rc = check_call(h, bufs, p, n, dtype, op, host_mapped);
     if (rc != RAR_OK) return rc;
     cudaStream_t stream = (cudaStream_t)stream_v;
@@ -316,6 +324,8 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         rc = fill_ptrs(h, a.bufs, bufs, p, stream);
         if (rc != RAR_OK) return rc;
         a.n = (long long)n;
+        a.first = g_first;
+        a.n_total = n_total;
         a.p = p;
         a.phase = phase;
         a.inv_p = inv_p;
@@ -380,18 +390,21 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     if (!hier) {
         const int first = phase == PHASE_AG ? p - 1 : 0;
         const int steps = phase == PHASE_ALL ? 2 * (p - 1) : p - 1;
-        return launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, bidir, RING_FLAT, p, first, steps, 0, stream);
+        return launch_ring_phase(h, ptrs, p, n, g_first, n_total, dtype, op, vec16, bidir, RING_FLAT, p, first, steps,
+                                 0, stream);
     }
     // "Ring All-Reduce, in depth", "Hierarchy": reduce-scatter inside the
     // nodes, all-reduce of each shard across the nodes, all-gather inside the
     // nodes -- three launches in stream order
     const int m = p / group;
-    rc = launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, false, RING_INTRA, group, 0, group - 1, 0, stream);
+    rc = launch_ring_phase(h, ptrs, p, n, g_first, n_total, dtype, op, vec16, false, RING_INTRA, group, 0, group - 1,
+                           0, stream);
     if (rc == RAR_OK)
-        rc = launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, false, RING_INTER, group, 0, 2 * (m - 1), 1, stream);
+        rc = launch_ring_phase(h, ptrs, p, n, g_first, n_total, dtype, op, vec16, false, RING_INTER, group, 0,
+                               2 * (m - 1), 1, stream);
     if (rc == RAR_OK)
-        rc = launch_ring_phase(h, ptrs, p, n, dtype, op, vec16, false, RING_INTRA, group, group - 1, group - 1, 2,
-                               stream);
+        rc = launch_ring_phase(h, ptrs, p, n, g_first, n_total, dtype, op, vec16, false, RING_INTRA, group, group - 1,
+                               group - 1, 2, stream);
     return rc;
 }
 
@@ -480,6 +493,15 @@ int rar_reduce_scatter(rar_handle h, void *const *bufs, int p, size_t n, int dty
 
 int rar_all_gather(rar_handle h, void *const *bufs, int p, size_t n, int dtype, void *stream) {
     return run(h, bufs, p, n, dtype, RAR_SUM, PHASE_AG, stream);
+}
+
+int rar_allreduce_range(rar_handle h, void *const *bufs, int p, size_t n_total, size_t lo, size_t hi, int dtype,
+                        int op, void *stream) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    if (lo > hi || hi > n_total) return fail(h, RAR_EINVAL, "the range needs lo <= hi <= n_total");
+    if (dtype >= RAR_INT32 && dtype <= RAR_FLOAT16 && n_total > (size_t)(1ull << 62) / (size_t)elem_bytes(dtype))
+        return fail(h, RAR_EINVAL, "n_total * element size overflows");
+    return run(h, bufs, p, hi - lo, dtype, op, PHASE_ALL, stream, false, (long long)lo, (long long)n_total);
 }
 
 int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bufs, int p, size_t n, int dtype,

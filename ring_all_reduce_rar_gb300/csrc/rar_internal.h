@@ -40,10 +40,18 @@ struct RingStatus {
     unsigned long long flag_wanted;
 };
 
-// Fused engines: one launch covers [0, n) of every rank.
+// Index ranges: the rank pointers may address element `first` of buffers
+// that hold `n_total` elements each; a launch then covers global indices
+// [first, first + n), and the chunks are cut from n_total, so the result is
+// that of the whole-buffer call on those indices.  first = 0 and
+// n_total = n for a whole-buffer call.
+
+// Fused engines: one launch covers [0, n) of every rank pointer.
 struct FusedArgs {
     RankPtrs bufs;
     long long n;
+    long long first;
+    long long n_total;
     int p;
     int phase;     // Phase
     float inv_p;   // binary32 nearest to 1/p
@@ -63,7 +71,9 @@ enum RingLayout {
 // Ring engines: persistent cooperative launch of p * channels CTAs.
 struct RingArgs {
     RankPtrs bufs;
-    long long n;
+    long long n;         // elements behind each rank pointer
+    long long first;     // global index of element 0 (see FusedArgs)
+    long long n_total;
     int p;
     int layout;          // RingLayout
     int group;           // ranks per node (RING_INTRA / RING_INTER)
@@ -72,7 +82,7 @@ struct RingArgs {
                          // forward ring on the first half, the rest the
                          // mirrored ring on the second half; == channels if
                          // not bidirectional
-    long long split;     // bidirectional: first index of the second half (n otherwise)
+    long long split;     // bidirectional: first global index of the second half (n_total otherwise)
     long long slice;     // elements per slice
     int first_step;      // global schedule steps [first_step, first_step + n_steps)
     int n_steps;

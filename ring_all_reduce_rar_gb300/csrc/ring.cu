@@ -29,6 +29,11 @@
 // [fwd_channels, channels) run the mirrored ring (send to r - 1) on the
 // second half of the buffer, cut by chunk_bounds(n, 2).
 //
+// Index ranges: a launch may cover global indices [first, first + n) of
+// buffers of n_total elements; chunks are cut from n_total and each hop moves
+// the part of its chunk inside the range, so the range gets the whole-buffer
+// result and schedule.
+//
 // Every wait is bounded (globaltimer and an iteration cap).  A CTA that runs
 // out records the failure in the status word, raises the abort word and
 // returns; the others see the abort word in their next wait and return.
@@ -115,22 +120,23 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
     const int GG = fwd ? a.fwd_channels : a.channels - a.fwd_channels;
     // this rank's ring: its size rp, its position in it, the global rank at
     // a position, and the segment of the buffer the ring works on
+    // (segments and chunks in global indices; see the clamp below)
     int rp = p, pos = r, ring_base = 0, ring_step = 1;
     long long seg_lo = fwd ? 0 : a.split;
-    long long L = fwd ? a.split : a.n - a.split;
+    long long L = fwd ? a.split : a.n_total - a.split;
     if (a.layout == RING_INTRA) {
         rp = a.group;
         pos = r % a.group;
         ring_base = r - pos;
         seg_lo = 0;
-        L = a.n;
+        L = a.n_total;
     } else if (a.layout == RING_INTER) {
         const int local = r % a.group;
         rp = p / a.group;
         pos = r / a.group;
         ring_base = local;
         ring_step = a.group;
-        const long long gb = a.n / a.group, ge = a.n % a.group;
+        const long long gb = a.n_total / a.group, ge = a.n_total % a.group;
         const int c = local + 1 == a.group ? 0 : local + 1;  // the shard this rank owns after the intra ring
         seg_lo = chunk_start(c, gb, ge);
         L = gb + (c < ge ? 1 : 0);
@@ -158,8 +164,13 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
             int c;
             if (fwd) c = rs ? mod_p(pos - 1 - s, rp) : mod_p(pos - s, rp);
             else c = rs ? mod_p(pos + 1 + s, rp) : mod_p(pos + s, rp);
-            const long long cs = seg_lo + chunk_start(c, base, extra);
-            const long long ce = seg_lo + chunk_start(c + 1, base, extra);
+            // the part of chunk c inside this launch's index range, in
+            // local indices (empty when the range misses the chunk)
+            const long long gl = a.first, gh = a.first + a.n;
+            long long cs = seg_lo + chunk_start(c, base, extra);
+            long long ce = seg_lo + chunk_start(c + 1, base, extra);
+            cs = (cs < gl ? gl : cs > gh ? gh : cs) - gl;
+            ce = (ce < gl ? gl : ce > gh ? gh : ce) - gl;
             const long long nsl = (ce - cs + a.slice - 1) / a.slice;
             const bool scale = scale_here && rs && s == rp - 2;  // this rank becomes the chunk's owner
             long long loc = 0;

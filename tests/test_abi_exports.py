@@ -31,7 +31,7 @@ def test_header_declares_the_api():
     names = declared_functions()
     for must in ("rar_init", "rar_allreduce", "rar_destroy", "rar_reduce_scatter", "rar_all_gather",
                  "rar_status", "rar_send_counts", "rar_last_error", "rar_set_options", "rar_version",
-                 "rar_allreduce_host"):
+                 "rar_allreduce_host", "rar_allreduce_range", "rar_allreduce_noalloc"):
         assert must in names
 
 
@@ -85,6 +85,7 @@ def test_host_side_errors_without_gpu(lib):
     assert lib.rar_destroy(None) == 0
     arr = (ctypes.c_void_p * 1)()
     assert lib.rar_allreduce(None, arr, 1, 4, 1, 0, None) == 1
+    assert lib.rar_allreduce_range(None, arr, 1, 8, 0, 4, 1, 0, None) == 1
     assert rar.rar_last_error(None) != ""
     h = ctypes.c_void_p()
     rc = lib.rar_init(ctypes.byref(h), 0, None)

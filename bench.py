@@ -155,7 +155,7 @@ def time_engine(rar, engine, rows, op, steps, warmup, dist_ctx):
     """Warm up, then time exactly `steps` all-reduces with CUDA events on the
     stream the kernels are launched on."""
     stream = torch.cuda.current_stream()
-    with rar.Handle(torch.cuda.current_device(), engine=engine, skip_pointer_check=True) as h:
+    with rar.Handle(torch.cuda.current_device(), skip_pointer_check=True, **VARIANTS[engine]) as h:
         for _ in range(warmup):
             h.allreduce(rows, op=op, stream=stream)
         h.check()
@@ -180,7 +180,7 @@ def time_e2e(rar, engine, host_rows, op, steps, warmup, dist_ctx):
     buffers: every step the GPU reads all p inputs from host memory and
     writes all p results back (rar_allreduce_host's zero-copy form)."""
     stream = torch.cuda.current_stream()
-    with rar.Handle(torch.cuda.current_device(), engine=engine, skip_pointer_check=True) as h:
+    with rar.Handle(torch.cuda.current_device(), skip_pointer_check=True, **VARIANTS[engine]) as h:
         def step():
             h.allreduce_host(host_rows, None, op=op, stream=stream)
         for _ in range(warmup):
@@ -335,6 +335,13 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ size sweep
 
+# Engine variants of the sweeps: "ring" picks its hand-off by size
+# (rar_options.protocol auto); "ring_simple" / "ring_ll" force one.
+VARIANTS = {"fused": dict(engine="fused"), "ring": dict(engine="ring"),
+            "ring_simple": dict(engine="ring", protocol="simple"), "ring_ll": dict(engine="ring", protocol="ll"),
+            "ring_bidir": dict(engine="ring_bidir"), "fused_tree": dict(engine="fused_tree"), "tree": dict(engine="tree")}
+
+
 def run_sweep(args):
     """Device time per call across message sizes (the p = 16 sweep workload),
     one JSON line per (engine, size).  The GPU is first held by a short sleep
@@ -347,12 +354,18 @@ def run_sweep(args):
     dtype, op, dist = w.SWEEP_PAIRS[args.pair]
     p = w.SWEEP_P
     e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
-    engines = ["fused", "ring", "ring_bidir", "tree"] if args.engine == "all" else [args.engine]
+    engines = (["fused", "ring", "ring_simple", "ring_ll", "ring_bidir", "tree"] if args.engine == "all"
+               else [args.engine])
     for n in w.SWEEP_SIZES:
         _, rows = w.make_inputs(p, n, dtype, dist, w.seed_of(w.SWEEP_INDEX), device=dev)
         k = 200 if n <= 4 ** 9 else 20
         for eng in engines:
-            us = device_us_per_call(rar, dict(engine=eng), rows, op, k)
+            try:
+                us = device_us_per_call(rar, VARIANTS[eng], rows, op, k)
+            except rar.RarError as ex:
+                if ex.code != 2:  # RAR_EUNSUPPORTED: e.g. too large for the low-latency mailbox
+                    raise
+                continue
             rb = (2 * p * n * e) if eng == "fused" else 5 * (p - 1) * n * e
             print(json.dumps({"sweep": f"p{p}_{dtype}_{op}", "engine": eng, "n": n, "us_per_call": round(us, 2),
                               "algbw_gbs": round(p * n * e / us / 1e3, 2),
@@ -389,8 +402,7 @@ def run_configs(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peak = hbm_peak()[0]
-    engines = [("fused", dict(engine="fused")), ("ring", dict(engine="ring")),
-               ("ring_bidir", dict(engine="ring_bidir")), ("tree", dict(engine="tree"))]
+    engines = [(e, VARIANTS[e]) for e in ("fused", "ring", "ring_simple", "ring_ll", "ring_bidir", "tree")]
     for name, cfg in w.WORKLOADS.items():
         p, n, dtype = cfg["p"], cfg["n"], cfg["dtype"]
         e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
@@ -398,7 +410,12 @@ def run_configs(args):
         for op in cfg["ops"]:
             for eng, opts in engines:
                 k = 10 if p * n * e > 1e9 else (50 if p * n * e > 1e7 else 200)
-                us = device_us_per_call(rar, opts, rows, op, k)
+                try:
+                    us = device_us_per_call(rar, opts, rows, op, k)
+                except rar.RarError as ex:
+                    if ex.code != 2:  # RAR_EUNSUPPORTED: too large for the low-latency mailbox
+                        raise
+                    continue
                 rb = 2 * p * n * e if eng == "fused" else 5 * (p - 1) * n * e
                 print(json.dumps({"workload": name, "op": op, "engine": eng, "us_per_call": round(us, 2),
                                   "algbw_gbs": round(p * n * e / us / 1e3, 2),
@@ -451,7 +468,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--engine", choices=["fused", "ring", "ring_bidir", "fused_tree", "tree", "all"], default="all")
+    ap.add_argument("--engine", choices=["fused", "ring", "ring_simple", "ring_ll", "ring_bidir", "fused_tree", "tree",
+                                         "all"], default="all")
     ap.add_argument("--sweep", action="store_true",
                     help="device time per call over the p = 16 message-size sweep (not the benchmark line)")
     ap.add_argument("--pair", type=int, default=0, help="--sweep: dtype/op pair of the sweep workload (0..2)")

@@ -137,10 +137,24 @@ typedef struct {
                                       inside each node.  Full all-reduce only; RAR_ENGINE_RING
                                       runs it as three ring launches, RAR_ENGINE_FUSED folds in
                                       its order on the per-thread path */
+    int protocol;                  /* RAR_ENGINE_RING hand-off, same results on both:
+                                      0 auto (low latency for small buffers);
+                                      1 progress words: a slice is published by a
+                                      release store after a fence, and the neighbour
+                                      reads it in place in the sender's buffer;
+                                      2 low latency: every 32-bit word travels with a
+                                      tag in one 64-bit store through a mailbox in the
+                                      handle's scratch (full all-reduce on the flat ring,
+                                      while p * 2 (p - 1) chunk-sized slots fit in
+                                      RAR_LL_MAILBOX_BYTES) */
 } rar_options;
 
+/* Bytes of the low-latency mailbox each handle allocates in rar_init. */
+#define RAR_LL_MAILBOX_BYTES (64u << 20)
+
 /* Create a handle on `device`; allocates the ring engines' flags, counters
- * and status word there (a few hundred KB).  opt may be NULL.
+ * and status word there (a few hundred KB) and the low-latency mailbox
+ * (RAR_LL_MAILBOX_BYTES).  opt may be NULL.
  * Errors: RAR_EINVAL (out NULL, bad device or option), RAR_ENOMEM,
  * RAR_ECUDA. */
 int rar_init(rar_handle *out, int device, const rar_options *opt);

@@ -18,6 +18,7 @@ OP_CODES = {"sum": 0, "max": 1, "avg": 2, "avg_prediv": 3}
 ENGINE_CODES = {"fused": 0, "ring": 1, "ring_bidir": 2, "fused_tree": 3, "tree": 4}
 FAULT_CODES = {"none": 0, "mute": 1, "delay": 2}
 FUSED_PATHS = {"auto": 0, "registers": 1, "stream": 2}
+PROTOCOLS = {"auto": 0, "simple": 1, "ll": 2}
 STATUS_NAMES = {0: "RAR_OK", 1: "RAR_EINVAL", 2: "RAR_EUNSUPPORTED", 3: "RAR_ENOMEM",
                 4: "RAR_ECUDA", 5: "RAR_ETIMEOUT", 6: "RAR_EABORTED"}
 RAR_MAX_P = 1024
@@ -45,12 +46,13 @@ class Options(ctypes.Structure):
         ("fault_delay_ns", ctypes.c_uint),
         ("fused_path", ctypes.c_int),
         ("hier_group", ctypes.c_int),
+        ("protocol", ctypes.c_int),
     ]
 
 
 def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, timeout_ns=0,
                  skip_pointer_check=False, fault_mode="none", fault_rank=0, fault_delay_ns=0,
-                 fused_path="auto", hier_group=0) -> Options:
+                 fused_path="auto", hier_group=0, protocol="auto") -> Options:
     o = Options()
     o.engine = ENGINE_CODES[engine] if isinstance(engine, str) else int(engine)
     o.channels = channels
@@ -63,6 +65,7 @@ def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, tim
     o.fault_delay_ns = fault_delay_ns
     o.fused_path = FUSED_PATHS[fused_path] if isinstance(fused_path, str) else int(fused_path)
     o.hier_group = hier_group
+    o.protocol = PROTOCOLS[protocol] if isinstance(protocol, str) else int(protocol)
     return o
 
 

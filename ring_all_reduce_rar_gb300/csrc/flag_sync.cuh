@@ -96,7 +96,7 @@ __device__ __forceinline__ unsigned launch_epoch_begin(const RingArgs &a) {
 
 // Every CTA calls this once, on every exit path, with all its threads.  The
 // last CTA to finish publishes the epoch for the next launch; on wrap-around
-// it first clears every progress word.
+// it first clears every progress word and mailbox word.
 __device__ __forceinline__ void launch_epoch_end(const RingArgs &a, unsigned epoch) {
     __shared__ int s_last;
     __syncthreads();
@@ -108,6 +108,7 @@ __device__ __forceinline__ void launch_epoch_end(const RingArgs &a, unsigned epo
     if (!s_last) return;
     if (epoch == 0xFFFFFFFFu) {
         for (int i = threadIdx.x; i < a.flag_capacity; i += blockDim.x) a.flags[i] = 0ull;
+        for (long long i = threadIdx.x; i < a.mailbox_words; i += blockDim.x) a.mailbox[i] = 0ull;
         __syncthreads();
     }
     if (threadIdx.x == 0) {

@@ -164,6 +164,9 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.finish_count = &scratch->finish_count;
     a.flag_capacity = kNoAllocMaxCtas;
     a.flags = scratch->flags;
+    a.mailbox = nullptr;
+    a.mailbox_words = 0;
+    a.slot_words = 0;
     a.recv_counts = scratch->recv_counts;
     a.status = &scratch->status;
     a.abort_word = &scratch->abort_word;

@@ -18,6 +18,10 @@ constexpr int kMaxRingCtas = 8192;           // flags / counters capacity
 constexpr int kRingPhases = 3;               // counter arrays: one per ring launch of a call
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr long long kMaxSlicesPerChannelStep = (1ll << 20) - 2;  // progress word field
+constexpr long long kLLMailboxWords = (long long)RAR_LL_MAILBOX_BYTES / 8;
+// protocol auto: the low-latency ring up to this many bytes per rank (p = 16
+// sweep on GB300: 31 us against 72 us at 4 KB per rank, 68 against 80 at 1 MB)
+constexpr size_t kLLAutoMaxBytes = (size_t)1 << 20;
 
 thread_local std::string g_init_error;  // errors before a handle exists
 
@@ -35,6 +39,7 @@ struct rar_ctx {
     unsigned *abort_word = nullptr;
     unsigned *epoch_words = nullptr;  // [0] last finished launch's epoch, [1] finish counter
     void **ptr_table = nullptr;
+    unsigned long long *ll_box = nullptr;  // low-latency mailbox, kLLMailboxWords
     unsigned acked_seq = 0;           // status failures already reported
     // last call, for rar_status / rar_send_counts
     bool have_last = false;
@@ -89,6 +94,7 @@ int check_options(rar_ctx *h, const rar_options &o) {
         return fail(h, RAR_EINVAL, "unknown fault_mode");
     if (o.fused_path < 0 || o.fused_path > 2) return fail(h, RAR_EINVAL, "unknown fused_path");
     if (o.hier_group < 0 || o.hier_group > RAR_MAX_P) return fail(h, RAR_EINVAL, "hier_group out of range");
+    if (o.protocol < 0 || o.protocol > 2) return fail(h, RAR_EINVAL, "unknown protocol");
     return RAR_OK;
 }
 
@@ -209,6 +215,9 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long lo
     a.finish_count = h->epoch_words + 1;
     a.flag_capacity = kMaxRingCtas;
     a.flags = h->flags;
+    a.mailbox = h->ll_box;
+    a.mailbox_words = kLLMailboxWords;
+    a.slot_words = 0;
     a.recv_counts = h->recv_counts + (size_t)phase_idx * kMaxRingCtas;
     a.status = h->status;
     a.abort_word = h->abort_word;
@@ -227,6 +236,70 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long lo
     h->last_fwd_channels[phase_idx] = fwd_channels;
     h->last_group = group;
     h->last_phases = phase_idx + 1;
+    return RAR_OK;
+}
+
+// Words per mailbox slot for the low-latency ring: the longest chunk part
+// of the launch, in 32-bit words; 0 if the mailbox cannot hold
+// p * 2 (p - 1) such slots.
+long long ll_slot_words(int p, size_t n, long long n_total, int dtype) {
+    const long long maxchunk = std::min((n_total + p - 1) / p, (long long)n);
+    const long long epw = 4 / elem_bytes(dtype);
+    const long long words = std::max<long long>(1, (maxchunk + epw - 1) / epw);
+    if ((long long)p * 2 * (p - 1) * words > kLLMailboxWords) return 0;
+    return words;
+}
+
+// The low-latency ring (full all-reduce, flat forward ring): enough CTAs per
+// rank for one word per thread and step, within the co-resident grid.
+int launch_ring_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long long g_first, long long n_total,
+                         int dtype, int op, long long slot_words, cudaStream_t stream) {
+    const int threads = ring_ll_threads();
+    const int max_ctas = std::min(ring_ll_max_coresident_ctas(dtype, op), kMaxRingCtas);
+    if (max_ctas < p) return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
+    int G = h->opt.channels;
+    if (G == 0) G = (int)std::min<long long>(max_ctas / p, (slot_words + threads - 1) / threads);
+    if ((long long)G * p > max_ctas) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
+    RingArgs a;
+    a.bufs = ptrs;
+    a.n = (long long)n;
+    a.first = g_first;
+    a.n_total = n_total;
+    a.p = p;
+    a.layout = RING_FLAT;
+    a.group = p;
+    a.channels = G;
+    a.fwd_channels = G;
+    a.split = n_total;
+    a.slice = 0;
+    a.first_step = 0;
+    a.n_steps = 2 * (p - 1);
+    a.inv_p = 1.0f / (float)p;
+    a.epoch_word = h->epoch_words;
+    a.finish_count = h->epoch_words + 1;
+    a.flag_capacity = kMaxRingCtas;
+    a.flags = h->flags;
+    a.mailbox = h->ll_box;
+    a.mailbox_words = kLLMailboxWords;
+    a.slot_words = slot_words;
+    a.recv_counts = h->recv_counts;
+    a.status = h->status;
+    a.abort_word = h->abort_word;
+    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
+    a.fault_mode = h->opt.fault_mode;
+    a.fault_rank = h->opt.fault_rank;
+    a.fault_delay_ns = h->opt.fault_delay_ns;
+    cudaError_t ce = launch_ring_ll(a, dtype, op, stream);
+    if (ce != cudaSuccess) {
+        if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "ring grid cannot be co-resident");
+        return cuda_fail(h, ce, "launching the low-latency ring");
+    }
+    h->last_ring = true;
+    h->last_layout[0] = RING_FLAT;
+    h->last_channels[0] = G;
+    h->last_fwd_channels[0] = G;
+    h->last_group = p;
+    h->last_phases = 1;
     return RAR_OK;
 }
 
@@ -270,6 +343,9 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     a.finish_count = h->epoch_words + 1;
     a.flag_capacity = kMaxRingCtas;
     a.flags = h->flags;
+    a.mailbox = h->ll_box;
+    a.mailbox_words = kLLMailboxWords;
+    a.slot_words = 0;
     a.recv_counts = h->recv_counts;
     a.status = h->status;
     a.abort_word = h->abort_word;
@@ -384,10 +460,21 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     const bool bidir = engine == RAR_ENGINE_RING_BIDIR;
     if (hier && (bidir || phase != PHASE_ALL))
         return fail(h, RAR_EUNSUPPORTED, "the hierarchical ring runs the full all-reduce on the forward ring only");
+    if (h->opt.protocol == 2 && (hier || bidir || phase != PHASE_ALL))
+        return fail(h, RAR_EUNSUPPORTED, "the low-latency protocol runs the full all-reduce on the flat forward ring");
     RankPtrs ptrs;
     rc = fill_ptrs(h, ptrs, bufs, p, stream);
     if (rc != RAR_OK) return rc;
     if (!hier) {
+        // hand-off protocol of the flat forward ring (rar_options.protocol)
+        const int proto = h->opt.protocol;
+        if (engine == RAR_ENGINE_RING && phase == PHASE_ALL && proto != 1) {
+            const long long slot_words = ll_slot_words(p, n, n_total, dtype);
+            if (proto == 2 && slot_words == 0)
+                return fail(h, RAR_EUNSUPPORTED, "the buffers are too large for the low-latency mailbox");
+            if (slot_words > 0 && (proto == 2 || n * (size_t)elem_bytes(dtype) <= kLLAutoMaxBytes))
+                return launch_ring_ll_phase(h, ptrs, p, n, g_first, n_total, dtype, op, slot_words, stream);
+        }
         const int first = phase == PHASE_AG ? p - 1 : 0;
         const int steps = phase == PHASE_ALL ? 2 * (p - 1) : p - 1;
         return launch_ring_phase(h, ptrs, p, n, g_first, n_total, dtype, op, vec16, bidir, RING_FLAT, p, first, steps,
@@ -449,13 +536,15 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
               cudaMalloc((void **)&h->status, sizeof(RingStatus)) == cudaSuccess &&
               cudaMalloc((void **)&h->abort_word, sizeof(unsigned)) == cudaSuccess &&
               cudaMalloc((void **)&h->epoch_words, 2 * sizeof(unsigned)) == cudaSuccess &&
-              cudaMalloc((void **)&h->ptr_table, sizeof(void *) * RAR_MAX_P) == cudaSuccess;
+              cudaMalloc((void **)&h->ptr_table, sizeof(void *) * RAR_MAX_P) == cudaSuccess &&
+              cudaMalloc((void **)&h->ll_box, sizeof(unsigned long long) * kLLMailboxWords) == cudaSuccess;
     if (ok) {
         ok = cudaMemset(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
              cudaMemset(h->recv_counts, 0, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
              cudaMemset(h->status, 0, sizeof(RingStatus)) == cudaSuccess &&
              cudaMemset(h->abort_word, 0, sizeof(unsigned)) == cudaSuccess &&
              cudaMemset(h->epoch_words, 0, 2 * sizeof(unsigned)) == cudaSuccess &&
+             cudaMemset(h->ll_box, 0, sizeof(unsigned long long) * kLLMailboxWords) == cudaSuccess &&
              cudaDeviceSynchronize() == cudaSuccess;
     }
     if (!ok) {
@@ -466,6 +555,7 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
         cudaFree(h->abort_word);
         cudaFree(h->epoch_words);
         cudaFree(h->ptr_table);
+        cudaFree(h->ll_box);
         delete h;
         return fail(nullptr, RAR_ENOMEM, "allocating the handle's scratch failed");
     }
@@ -637,6 +727,7 @@ int rar_destroy(rar_handle h) {
         cudaFree(h->abort_word);
         cudaFree(h->epoch_words);
         cudaFree(h->ptr_table);
+        cudaFree(h->ll_box);
     }
     delete h;
     return RAR_OK;

@@ -194,10 +194,9 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
                     received += (unsigned long long)(hi - lo);
                 }
                 __syncthreads();
-                if (threadIdx.x == 0) {
-                    __threadfence();
-                    st_release_u64(my_flag, progress_tag(epoch, step, loc));
-                }
+                // the release store orders the CTA's slice stores (ordered
+                // before it by the barrier) ahead of the progress word
+                if (threadIdx.x == 0) st_release_u64(my_flag, progress_tag(epoch, step, loc));
             }
         }
     }

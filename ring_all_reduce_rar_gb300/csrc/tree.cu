@@ -86,10 +86,7 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __
         }
         if (peer < 0) {
             // nothing to do: the step is passed as soon as the previous one is
-            if (threadIdx.x == 0) {
-                __threadfence();
-                st_release_u64(my_flag, progress_tag(epoch, t, kTreePassLoc));
-            }
+            if (threadIdx.x == 0) st_release_u64(my_flag, progress_tag(epoch, t, kTreePassLoc));
             continue;
         }
         const char *src = rank_ptr(a.bufs, p, peer);
@@ -110,9 +107,10 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __
             const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
             tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, root_last, a.inv_p);
             __syncthreads();
+            // the release store orders the CTA's slice stores (ordered
+            // before it by the barrier) ahead of the progress word
             if (threadIdx.x == 0) {
                 atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // elements the peer sent
-                __threadfence();
                 st_release_u64(my_flag, progress_tag(epoch, t, loc));
             }
         }

@@ -17,9 +17,15 @@ pytestmark = pytest.mark.gpu
 
 RING_ENGINES = ["fused", "fused_regs", "fused_stream", "ring", "ring_bidir"]
 # "fused_regs" / "fused_stream" force the fused engine's per-thread or
-# streaming (bulk-copy) data path; "fused" lets the library choose
+# streaming (bulk-copy) data path; "fused" lets the library choose.  "ring"
+# is the ring executor with progress words; "ring_ll" the same schedule with
+# the low-latency hand-off (tests/test_gpu_ll.py).
+# small-buffer tests also run the low-latency ring
+SMALL_ENGINES = RING_ENGINES + ["ring_ll"]
 ENGINE_OPTS = {"fused_regs": dict(engine="fused", fused_path="registers"),
-               "fused_stream": dict(engine="fused", fused_path="stream")}
+               "fused_stream": dict(engine="fused", fused_path="stream"),
+               "ring": dict(engine="ring", protocol="simple"),
+               "ring_ll": dict(engine="ring", protocol="ll")}
 
 
 def handle_opts(engine, **opts):
@@ -87,7 +93,7 @@ def run_case(rar, dev, host_rows, dtype, op, engine, offset=0, **opts):
     torch.cuda.synchronize()
     assert_bits_equal(rows, ref, f"{engine} {dtype} {op} p={len(rows)} n={rows[0].numel()}")
     p, n = len(rows), rows[0].numel()
-    if engine in ("ring", "ring_bidir"):
+    if engine in ("ring", "ring_ll", "ring_bidir"):
         assert list(got_sends) == list(sends)
     elif engine == "tree":
         assert sum(got_sends) == 2 * (p - 1) * n
@@ -102,7 +108,7 @@ def gen(p, n, dtype, dist, seed):
 
 # ----------------------------------------------------------------- page cases
 
-@pytest.mark.parametrize("engine", RING_ENGINES + ["fused_tree"])
+@pytest.mark.parametrize("engine", SMALL_ENGINES + ["fused_tree"])
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
 def test_page_trace_p4_n4(rar, dev, engine, dtype):
     """"Ring All-Reduce, in depth", "Tracing four GPUs": [10, 100, 1000, 10000]
@@ -122,11 +128,11 @@ def test_page_trace_p4_n4(rar, dev, engine, dtype):
     else:
         for t in rows:
             assert t.float().tolist() == [10.0, 100.0, 1000.0, 10000.0]
-    if engine == "ring":
+    if engine in ("ring", "ring_ll"):
         assert sends == [6, 6, 6, 6]
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_semantics_example_p4_n1(rar, dev, engine):
     """"AllReduce 与 Ring 通信算法详解": [1, 2, 3, 4] -> 10 everywhere (N < p)."""
     host = [torch.tensor([float(r + 1)]) for r in range(4)]
@@ -136,13 +142,13 @@ def test_semantics_example_p4_n1(rar, dev, engine):
         h.check()
         sends = h.send_counts(4)
     assert [t.item() for t in rows] == [10.0] * 4
-    if engine == "ring":
+    if engine in ("ring", "ring_ll"):
         assert sends == [2, 2, 1, 1]
 
 
 # ----------------------------------------------------------------- workloads
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_p4_n4099_f32_uniform_sum(rar, dev, engine):
     cfg = w.WORKLOADS["p4_n4099_f32"]
     host = gen(cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"]))
@@ -157,7 +163,7 @@ def test_p8_n6553600_f32_normal(rar, dev, engine, op):
     run_case(rar, dev, host, "float32", op, engine)
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_p64_bf16_full_compare_reduced_n(rar, dev, engine):
     """p = 64 bf16 (large-p case) at a size the oracle runs element by
     element: 64 chunks of ~1000 elements plus a ragged tail."""
@@ -227,7 +233,7 @@ def test_p8_n2pow30_bf16_full_size_sampled(rar, dev, engine):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 @pytest.mark.parametrize("pair", range(3))
 def test_p16_sweep(rar, dev, engine, pair):
     """p = 16, N = 4^5 .. 4^13: int32 sum, fp32 max, fp32 avg.  Element by
@@ -236,6 +242,8 @@ def test_p16_sweep(rar, dev, engine, pair):
     seed = w.seed_of(w.SWEEP_INDEX) + 16 * pair
     p = w.SWEEP_P
     for n in w.SWEEP_SIZES:
+        if engine == "ring_ll" and n > 4 ** 8:
+            break  # larger buffers do not fit the low-latency mailbox
         if n <= 4 ** 10:
             host = gen(p, n, dtype, dist, seed)
             run_case(rar, dev, host, dtype, op, engine)
@@ -249,7 +257,7 @@ def test_p16_sweep(rar, dev, engine, pair):
 
 # ----------------------------------------------------------------- edge cases
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_odd_p_ragged_n_and_small_n(rar, dev, engine):
     """Runtime-p paths (p not 4/8/16), N < p (empty chunks), ragged tails."""
     for p in [2, 3, 5, 7, 13, 31]:
@@ -260,7 +268,7 @@ def test_odd_p_ragged_n_and_small_n(rar, dev, engine):
             run_case(rar, dev, host, "float32", "sum", engine)
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 @pytest.mark.parametrize("dtype,op", [("int32", "max"), ("bfloat16", "max"), ("bfloat16", "avg"),
                                       ("float16", "sum"), ("float16", "avg"), ("float16", "max"),
                                       ("int32", "sum"), ("float32", "max"), ("float32", "avg_prediv"),
@@ -272,7 +280,7 @@ def test_dtype_op_matrix(rar, dev, engine, dtype, op):
         run_case(rar, dev, host, dtype, op, engine)
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_misaligned_pointers_take_element_path(rar, dev, engine):
     """Rank pointers offset by one element (not 16-byte aligned): same bits."""
     for dtype in ["float32", "bfloat16"]:
@@ -280,7 +288,7 @@ def test_misaligned_pointers_take_element_path(rar, dev, engine):
         run_case(rar, dev, host, dtype, "sum", engine, offset=1)
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_large_p_uses_pointer_table(rar, dev, engine):
     """p > 64: rank pointers travel through the device-side table."""
     p = 96 if engine == "fused" else 72
@@ -297,7 +305,7 @@ def test_largest_p(rar, dev, engine):
     run_case(rar, dev, host, "float32", "sum", engine)
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES)
+@pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_trivial_calls(rar, dev, engine):
     one = [torch.arange(10, dtype=torch.float32, device=dev)]
     empty = [torch.zeros(0, device=dev) for _ in range(4)]
@@ -312,18 +320,18 @@ def test_fp32_special_values(rar, dev):
     """Subnormals survive (no flush to zero), overflow goes to inf, -0 kept."""
     tiny = np.float32(1e-45)
     host = [torch.tensor([tiny, 3e38, -0.0, 1.0] * 8, dtype=torch.float32) for _ in range(4)]
-    for engine in RING_ENGINES:
+    for engine in SMALL_ENGINES:
         run_case(rar, dev, host, "float32", "sum", engine)
 
 
 def test_bf16_subnormals_and_ties(rar, dev):
     vals = np.array([0x0001, 0x0080, 0x8001, 0x3F80, 0x3B80, 0x4380, 0x7F7F] * 9, dtype=np.uint16)
     host = [torch.from_numpy(np.roll(vals, r).astype(np.int16)).view(torch.bfloat16) for r in range(5)]
-    for engine in RING_ENGINES:
+    for engine in SMALL_ENGINES:
         run_case(rar, dev, host, "bfloat16", "sum", engine)
 
 
-@pytest.mark.parametrize("engine", RING_ENGINES + ["fused_tree"])
+@pytest.mark.parametrize("engine", SMALL_ENGINES + ["fused_tree"])
 def test_prediv_fp16_no_overflow(rar, dev, engine):
     """16 ranks of fp16 4096: the post-divided average overflows to inf (the
     sum 65536 exceeds 65504), the pre-divided one is exactly 4096."""
@@ -349,7 +357,7 @@ def test_ring_race_check_slices_and_channels(rar, dev):
         r2 = oracle_expect(host, "bfloat16", "sum", engine)[0]
         for ch, sl, bt in [(1, 16, 128), (2, 64, 256), (3, 1024, 512), (7, 4096, 512), (16, 160, 64)]:
             _, rows = upload(host, dev)
-            with rar.Handle(0, engine=engine, channels=ch, slice_elems=sl, block_threads=bt) as h:
+            with rar.Handle(0, **handle_opts(engine, channels=ch, slice_elems=sl, block_threads=bt)) as h:
                 h.allreduce(rows)
                 h.check()
             assert_bits_equal(rows, r2 if engine == "ring_bidir" else ref, f"{engine} ch={ch} sl={sl}")
@@ -358,7 +366,7 @@ def test_ring_race_check_slices_and_channels(rar, dev):
 def test_ring_back_to_back_calls_reuse_flags(rar, dev):
     host = gen(4, 4099, "float32", ("uniform", -1.0, 1.0), 3)
     ref, _ = oracle_expect(host, "float32", "sum", "ring")
-    with rar.Handle(0, engine="ring") as h:
+    with rar.Handle(0, **handle_opts("ring")) as h:
         for _ in range(5):
             _, rows = upload(host, dev)
             h.allreduce(rows)
@@ -373,12 +381,12 @@ def test_ring_muted_rank_times_out_and_handle_recovers(rar, dev, engine):
     succeeds (the context stays usable)."""
     host = gen(4, 4 * 4096, "float32", ("normal", 1.0), 9)
     _, rows = upload(host, dev)
-    with rar.Handle(0, engine=engine, timeout_ns=50_000_000, fault_mode="mute", fault_rank=2,
-                    slice_elems=512) as h:
+    with rar.Handle(0, **handle_opts(engine, timeout_ns=50_000_000, fault_mode="mute", fault_rank=2,
+                                     slice_elems=512)) as h:
         h.allreduce(rows)
         assert h.status() == 5  # RAR_ETIMEOUT
         assert "timed out" in rar.rar_last_error(h.h)
-        h.set_options(engine=engine)
+        h.set_options(**handle_opts(engine))
         ref, _ = oracle_expect(host, "float32", "sum", engine)
         _, rows = upload(host, dev)
         h.allreduce(rows)
@@ -551,7 +559,7 @@ def test_tree_executor_fault_and_rejections(rar, dev):
 
 # ----------------------------------------------------------------- CUDA graphs
 
-@pytest.mark.parametrize("engine,opts", [("fused_regs", {}), ("fused_stream", {}), ("ring", {}),
+@pytest.mark.parametrize("engine,opts", [("fused_regs", {}), ("fused_stream", {}), ("ring", {}), ("ring_ll", {}),
                                          ("ring_bidir", {}), ("tree", {}), ("ring", dict(hier_group=2)),
                                          ("fused_tree", {})])
 def test_captured_call_replays(rar, dev, engine, opts):
@@ -584,7 +592,7 @@ def test_captured_call_replays(rar, dev, engine, opts):
 
 # ----------------------------------------------------------------- host buffers
 
-@pytest.mark.parametrize("engine", ["fused", "fused_stream", "ring"])
+@pytest.mark.parametrize("engine", ["fused", "fused_stream", "ring", "ring_ll"])
 def test_allreduce_host_pinned_and_pageable(rar, dev, engine):
     """rar_allreduce_host: pinned host buffers are reduced in place by the GPU
     (zero copy); pageable ones are staged through device buffers.  Both equal

@@ -419,21 +419,31 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         }
         // data path: per-thread 128-bit loads ("registers") or the
         // rank-sequential bulk-copy streaming path.  Auto (measured on GB300):
-        // registers for p <= 16 below 80 MB per rank, streaming otherwise.
+        // registers for p <= 16 below 256 MB over all ranks, streaming
+        // otherwise (p = 8 fp32: 0.90 against 0.88 at 25 MB per rank, 0.92
+        // against 0.95 at 48 MB; p = 16: tied at 16 MB per rank).
         const size_t bytes = n * (size_t)elem_bytes(dtype);
         const bool stream_ok = engine == RAR_ENGINE_FUSED && phase == PHASE_ALL && vec16;
         int path = h->opt.fused_path;
         if (path == 2 && !stream_ok)
             return fail(h, RAR_EUNSUPPORTED,
                         "the streaming path needs engine fused, a full all-reduce and 16-byte aligned rank buffers");
-        if (path == 0) path = (stream_ok && (p > 16 || bytes >= (size_t)80 << 20)) ? 2 : 1;
+        if (path == 0) path = (stream_ok && (p > 16 || (size_t)p * bytes >= (size_t)256 << 20)) ? 2 : 1;
         if (path == 2) {
-            // tile per rank (slice_elems, else 32 KB, halved while there are
-            // fewer than four tiles per SM); stages (channels, else 3)
-            size_t tb = h->opt.slice_elems ? (size_t)h->opt.slice_elems * (size_t)elem_bytes(dtype) : 32768;
-            tb = std::min<size_t>(std::max<size_t>(tb / 512 * 512, 512), 32768);
-            if (!h->opt.slice_elems)
-                while (tb > 512 && bytes / tb < (size_t)(4 * h->sm_count)) tb /= 2;
+            // tile per rank: slice_elems, else the largest tile up to 32 KB
+            // (a multiple of 512 bytes) that cuts the buffer into k rounds of
+            // one tile per CTA (one CTA per SM), k >= 4, with the last round
+            // nearly full; stages: channels, else 3
+            size_t tb;
+            if (h->opt.slice_elems) {
+                tb = (size_t)h->opt.slice_elems * (size_t)elem_bytes(dtype);
+                tb = std::min<size_t>(std::max<size_t>(tb / 512 * 512, 512), 32768);
+            } else {
+                const size_t sms = (size_t)h->sm_count;
+                const size_t rounds = std::max<size_t>(4, (bytes + 32768 * sms - 1) / (32768 * sms));
+                tb = (bytes + rounds * sms - 1) / (rounds * sms);
+                tb = std::min<size_t>(std::max<size_t>((tb + 511) / 512 * 512, 512), 32768);
+            }
             const int stages = h->opt.channels ? h->opt.channels : 3;
             if (stages < 2 || stages > 8 || (size_t)(stages + 2) * tb > 227 * 1024)
                 return fail(h, RAR_EINVAL, "streaming path: stages (channels) must be in [2, 8] and fit in 227 KB");

@@ -7,6 +7,9 @@ ranks, N = 2^30 bf16 elements per rank (16 GiB in total, far above the
 
     python bench.py [--steps K] [--warmup W] [--engine fused|ring|ring_bidir|all]
     python bench.py --impl reference      # the CPU oracle on the host cores
+    python bench.py --sweep [--pair 0|1|2] # p = 16, N = 4^5 ... 4^13, every engine
+    python bench.py --configs             # every workload on every engine
+    python bench.py --hops                # smallest buffers, p = 2 ... 64
 
 Metric: algBW = p * N * element bytes / time per step (GB/s), summed over
 GPUs when run under torchrun (independent replicas, weak scaling).  Also
@@ -335,11 +338,12 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ size sweep
 
-# Engine variants of the sweeps: "ring" picks its hand-off by size
-# (rar_options.protocol auto); "ring_simple" / "ring_ll" force one.
+# Engine variants of the sweeps: "ring" and "tree" pick their hand-off by
+# size (rar_options.protocol auto); the "_simple" / "_ll" variants force one.
 VARIANTS = {"fused": dict(engine="fused"), "ring": dict(engine="ring"),
             "ring_simple": dict(engine="ring", protocol="simple"), "ring_ll": dict(engine="ring", protocol="ll"),
-            "ring_bidir": dict(engine="ring_bidir"), "fused_tree": dict(engine="fused_tree"), "tree": dict(engine="tree")}
+            "ring_bidir": dict(engine="ring_bidir"), "fused_tree": dict(engine="fused_tree"), "tree": dict(engine="tree"),
+            "tree_simple": dict(engine="tree", protocol="simple"), "tree_ll": dict(engine="tree", protocol="ll")}
 
 
 def run_sweep(args):
@@ -354,8 +358,8 @@ def run_sweep(args):
     dtype, op, dist = w.SWEEP_PAIRS[args.pair]
     p = w.SWEEP_P
     e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
-    engines = (["fused", "ring", "ring_simple", "ring_ll", "ring_bidir", "tree"] if args.engine == "all"
-               else [args.engine])
+    engines = (["fused", "ring", "ring_simple", "ring_ll", "ring_bidir", "tree", "tree_simple", "tree_ll"]
+               if args.engine == "all" else [args.engine])
     for n in w.SWEEP_SIZES:
         _, rows = w.make_inputs(p, n, dtype, dist, w.seed_of(w.SWEEP_INDEX), device=dev)
         k = 200 if n <= 4 ** 9 else 20
@@ -372,6 +376,25 @@ def run_sweep(args):
                               "roofline_frac": round(rb / us / 1e3 / hbm_peak()[0], 4)}), flush=True)
         del rows
         torch.cuda.empty_cache()
+
+
+def run_hops(args):
+    """Per-call time of the smallest buffers (N = 64 p fp32 elements per
+    rank) for p = 2 ... 64: with the data negligible, the time is the fixed
+    cost of a call plus the schedule's steps (2 (p - 1) ring hops,
+    2 ceil(log2 p) tree steps), for each hand-off.  One JSON line per p."""
+    import ring_all_reduce_rar_gb300 as rar
+    rar.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for p in [2, 4, 8, 16, 32, 64]:
+        n = 64 * p
+        _, rows = w.make_inputs(p, n, "float32", ("normal", 1.0), w.seed_of(w.SWEEP_INDEX), device=dev)
+        line = {"hops": f"p{p}_n{n}_float32", "p": p, "n": n, "ring_steps": 2 * (p - 1),
+                "tree_steps": 2 * max(1, (p - 1).bit_length())}
+        for eng in ["fused", "ring_simple", "ring_ll", "tree_simple", "tree_ll"]:
+            line[eng + "_us"] = round(device_us_per_call(rar, VARIANTS[eng], rows, "sum", 200), 2)
+        print(json.dumps(line), flush=True)
 
 
 def device_us_per_call(rar, opts, rows, op, k):
@@ -469,10 +492,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--engine", choices=["fused", "ring", "ring_simple", "ring_ll", "ring_bidir", "fused_tree", "tree",
-                                         "all"], default="all")
+                                         "tree_simple", "tree_ll", "all"], default="all")
     ap.add_argument("--sweep", action="store_true",
                     help="device time per call over the p = 16 message-size sweep (not the benchmark line)")
     ap.add_argument("--pair", type=int, default=0, help="--sweep: dtype/op pair of the sweep workload (0..2)")
+    ap.add_argument("--hops", action="store_true",
+                    help="per-call time of the smallest buffers for p = 2 ... 64 (fixed cost + step latency)")
     ap.add_argument("--configs", action="store_true",
                     help="device time per call of every workload on every engine (not the benchmark line)")
     ap.add_argument("--workload", choices=sorted(w.WORKLOADS), default="p8_n1073741824_bf16")
@@ -485,6 +510,8 @@ def main():
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.sweep:
         run_sweep(args)
+    elif args.hops:
+        run_hops(args)
     elif args.configs:
         run_configs(args)
     elif args.impl == "reference":

@@ -137,16 +137,18 @@ typedef struct {
                                       inside each node.  Full all-reduce only; RAR_ENGINE_RING
                                       runs it as three ring launches, RAR_ENGINE_FUSED folds in
                                       its order on the per-thread path */
-    int protocol;                  /* RAR_ENGINE_RING hand-off, same results on both:
+    int protocol;                  /* RAR_ENGINE_RING and RAR_ENGINE_TREE hand-off, same
+                                      results on both:
                                       0 auto (low latency for small buffers);
                                       1 progress words: a slice is published by a
-                                      release store after a fence, and the neighbour
-                                      reads it in place in the sender's buffer;
+                                      release store, and the receiver reads it in place
+                                      in the sender's buffer;
                                       2 low latency: every 32-bit word travels with a
                                       tag in one 64-bit store through a mailbox in the
-                                      handle's scratch (full all-reduce on the flat ring,
-                                      while p * 2 (p - 1) chunk-sized slots fit in
-                                      RAR_LL_MAILBOX_BYTES) */
+                                      handle's scratch.  Ring: full all-reduce on the flat
+                                      ring, while p * 2 (p - 1) chunk-sized slots fit in
+                                      RAR_LL_MAILBOX_BYTES; tree: while
+                                      p * (ceil(log2 p) + 1) buffer-sized slots fit */
 } rar_options;
 
 /* Bytes of the low-latency mailbox each handle allocates in rar_init. */
@@ -268,6 +270,15 @@ int rar_destroy(rar_handle h);
 
 /* RAR_VERSION of the loaded library. */
 int rar_version(void);
+
+/* Test hook: set the handle's launch epoch counter (device memory; the next
+ * ring-engine or tree launch runs with epoch + 1).  The ring engines tag
+ * progress words and mailbox words with a 32-bit epoch; the launch that runs
+ * with epoch 0xFFFFFFFF clears them all and restarts the count, so no stale
+ * tag can match.  This call lets a test reach that launch without 2^32
+ * calls.  Synchronises the device; no call may be in flight.
+ * Errors: RAR_EINVAL (null handle), RAR_ECUDA. */
+int rar_debug_set_epoch(rar_handle h, unsigned epoch);
 
 #ifdef __cplusplus
 }

@@ -10,7 +10,8 @@ over device pointers and streams.
 """
 from ._abi import (DTYPE_CODES, ENGINE_CODES, FAULT_CODES, OP_CODES, RAR_MAX_P, STATUS_NAMES, Handle, Options,
                    RarError, library_path, load_library, make_options, rar_all_gather, rar_allreduce,
-                   rar_allreduce_host, rar_allreduce_noalloc, rar_allreduce_ptrs, rar_allreduce_range, rar_destroy,
+                   rar_allreduce_host, rar_allreduce_noalloc, rar_allreduce_ptrs, rar_allreduce_range, rar_debug_set_epoch,
+                   rar_destroy,
                    rar_init, rar_last_error, rar_reduce_scatter, rar_send_counts, rar_set_options, rar_status,
                    rar_version)
 from ._build import build
@@ -18,7 +19,8 @@ from ._build import build
 __all__ = [
     "DTYPE_CODES", "ENGINE_CODES", "FAULT_CODES", "OP_CODES", "RAR_MAX_P", "STATUS_NAMES", "Handle", "Options",
     "RarError", "build", "library_path", "load_library", "make_options", "rar_all_gather", "rar_allreduce",
-    "rar_allreduce_host", "rar_allreduce_noalloc", "rar_allreduce_ptrs", "rar_allreduce_range", "rar_destroy",
+    "rar_allreduce_host", "rar_allreduce_noalloc", "rar_allreduce_ptrs", "rar_allreduce_range", "rar_debug_set_epoch",
+    "rar_destroy",
     "rar_init", "rar_last_error", "rar_reduce_scatter", "rar_send_counts", "rar_set_options", "rar_status",
     "rar_version",
 ]

@@ -103,8 +103,9 @@ def load_library():
         lib.rar_last_error.restype = ctypes.c_char_p
         lib.rar_destroy.argtypes = [vp]
         lib.rar_version.argtypes = []
+        lib.rar_debug_set_epoch.argtypes = [vp, ctypes.c_uint]
         for name in ("rar_init", "rar_set_options", "rar_allreduce", "rar_reduce_scatter",
-                     "rar_all_gather", "rar_allreduce_range", "rar_allreduce_host", "rar_allreduce_noalloc", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
+                     "rar_all_gather", "rar_allreduce_range", "rar_allreduce_host", "rar_debug_set_epoch", "rar_allreduce_noalloc", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -241,6 +242,11 @@ def rar_send_counts(handle: int, p: int) -> list[int]:
 
 def rar_last_error(handle: int | None) -> str:
     return load_library().rar_last_error(handle).decode(errors="replace")
+
+
+def rar_debug_set_epoch(handle: int, epoch: int) -> None:
+    """Test hook (see rar_debug_set_epoch in rar.h)."""
+    _check(handle, load_library().rar_debug_set_epoch(handle, epoch))
 
 
 def rar_destroy(handle: int) -> None:

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "librar.so")
 
-SOURCES = ["rar_api.cu", "fused.cu", "fused_stream.cu", "ring.cu", "ring_ll.cu", "tree.cu", "noalloc.cu"]
+SOURCES = ["rar_api.cu", "fused.cu", "fused_stream.cu", "ring.cu", "ll.cu", "tree.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=false", "-prec-div=true",
               "-prec-sqrt=true", "-fmad=false", "-Xptxas", "-warn-spills", "-I", INCLUDE, "-I", CSRC]

@@ -1,12 +1,12 @@
-// ring_ll.cu -- the ring schedule with a low-latency hand-off, for small
-// buffers.
+// ll.cu -- the ring and tree schedules with a low-latency hand-off, for
+// small buffers.
 //
-// The ring executor (ring.cu) hands a slice over through a progress word:
-// the sender makes its stores visible (a fence), publishes the word, and the
-// receiver polls the word and only then reads the data.  A hop thus costs
-// several round trips to L2 -- about 2 us on GB300 -- and for small buffers
-// the 2 (p - 1) hops are the whole cost ("Derive the cost of a ring
-// all-reduce": the latency term grows with p).
+// The ring and tree executors (ring.cu, tree.cu) hand a slice over through a
+// progress word: the sender's release store publishes it after its slice
+// stores, and the receiver polls the word and only then reads the data.  A
+// hop thus costs several round trips to L2 -- about 2 us on GB300 -- and
+// for small buffers the hops are the whole cost ("Derive the cost of a ring
+// all-reduce": the latency term grows with the number of steps).
 //
 // Here every 32-bit word of a message travels with a 32-bit tag, the
 // launch's epoch, in one aligned 64-bit store, which a reader sees whole or
@@ -14,20 +14,21 @@
 // separate flag, no CTA barrier, so a hop costs about one store-to-load trip.
 //
 // Messages go through a mailbox in the handle's scratch with one slot per
-// (receiving rank, schedule step), each as long as the largest chunk, so a
-// sender never overwrites a message that its receiver has not read yet, and
-// a rank never waits for anything but its left neighbour.  The schedule, the
-// chunks, the fold order and the owner's epilogue are the ring executor's
-// ("Ring All-Reduce, in depth", "The schedule"), so results and send counts
-// are identical bit for bit.  Rank buffers are read once (own inputs) and
-// written once (final values); partial sums live only in the mailbox, so the
-// traffic is about twice the in-place executor's: this is a latency path.
+// (receiving rank, message), so a sender never overwrites a message that its
+// receiver has not read yet, and a rank only ever waits for the ranks the
+// schedule makes it wait for.  Schedules, fold orders and epilogues are the
+// executors' ("Ring All-Reduce, in depth", "The schedule"; the tree of
+// "Derive the cost of a ring all-reduce"), so results and send counts are
+// identical bit for bit.  Rank buffers are read once (own inputs) and written
+// once (final values); partial sums live only in the mailbox, so the traffic
+// is about twice the in-place executors': this is a latency path.
 //
-// Word w of a chunk holds the chunk's element w (32-bit types) or elements
-// 2w and 2w + 1 (16-bit types).  Thread w mod (channels x blockDim) of every
-// rank handles word w at every step, so each thread is an independent chain
-// around the ring.  Every wait is bounded; a wait that runs out records the
-// failure in the status word and raises the abort word, like the executor's.
+// Word w holds element w (32-bit types) or elements 2w and 2w + 1 (16-bit
+// types) of a chunk (ring) or of the buffer (tree).  Thread
+// w mod (channels x blockDim) of every rank handles word w at every step, so
+// each thread is an independent chain through the schedule.  Every wait is
+// bounded; a wait that runs out records the failure in the status word and
+// raises the abort word, like the executors'.
 #include "flag_sync.cuh"
 
 namespace rar {
@@ -197,6 +198,113 @@ done:
     launch_epoch_end(a, epoch);
 }
 
+// The tree all-reduce (tree.cu's schedule and order) with tagged words.
+// L = ceil(log2 p).  Rank r > 0 sends up at level ls = (lowest set bit of r)
+// to its parent r - 2^ls, after folding in its children r + 2^l, l < ls
+// (the root: all levels); each partial is acc = op(acc, child), the lower
+// ranks on the left.  The root scales avg; then the final value travels
+// down: each rank waits for its parent's word and passes it on to its
+// children from the highest level down.  Mailbox slots per rank: one per
+// up level (0 .. L-1) and one for the down message (L).
+template <int DT, int OP>
+__global__ void __launch_bounds__(kLLThreads) tree_ll_kernel(const __grid_constant__ RingArgs a) {
+    __shared__ unsigned long long s_sent;
+    constexpr int EPW = 4 / ElemInfo<DT>::bytes;
+    constexpr int hop_op = HopOf<OP>::value;
+    const int p = a.p;
+    const int r = blockIdx.x / a.channels;
+    const int j = blockIdx.x % a.channels;
+    const long long gt = (long long)j * blockDim.x + threadIdx.x;
+    const long long GT = (long long)a.channels * blockDim.x;
+    int L = 0;
+    while ((1 << L) < p) L++;
+    const int ls = r == 0 ? L : __ffs(r) - 1;  // the level r sends up at (the root: none)
+    const int parent = r == 0 ? 0 : r - (1 << ls);
+    char *own = rank_ptr(a.bufs, p, r);
+    const long long n = a.n;
+    const long long words = (n + EPW - 1) / EPW;
+    auto slot = [&](int rank, int k) { return a.mailbox + ((long long)rank * (L + 1) + k) * a.slot_words; };
+    if (threadIdx.x == 0) s_sent = 0;
+    const unsigned epoch = launch_epoch_begin(a);  // (its barrier also orders s_sent)
+    const unsigned long long tag = (unsigned long long)epoch << 32;
+    unsigned long long sent = 0;
+    const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
+    const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
+
+    if (!muted) {
+        for (long long w0 = gt; w0 < words; w0 += GT * kLLBatch) {
+            const long long left = (words - w0 + GT - 1) / GT;
+            const int nbw = left < kLLBatch ? (int)left : kLLBatch;  // words of this batch
+            uint32_t acc[kLLBatch];
+            unsigned long long v[kLLBatch];
+            long long elems = 0;  // elements in this batch's words
+#pragma unroll
+            for (int b = 0; b < kLLBatch; b++) {
+                if (b < nbw) {
+                    const long long e0 = (w0 + b * GT) * EPW;
+                    acc[b] = ll_load_word<DT>(own, e0, n);
+                    elems += n - e0 < EPW ? n - e0 : EPW;
+                }
+            }
+            // reduce: fold in each child's partial, lowest level first
+            for (int l = 0; l < ls; l++) {
+                const int child = r + (1 << l);
+                if (child >= p) break;  // higher levels' children are farther still
+                if (slow) ring_delay(a.fault_delay_ns);
+                const unsigned long long *in = slot(r, l);
+#pragma unroll
+                for (int b = 0; b < kLLBatch; b++)
+                    if (b < nbw) v[b] = ld_relaxed_u64(in + w0 + b * GT);
+                if (!ll_wait_batch(a, epoch, in, w0, GT, nbw, v, r, l, child)) goto done;
+#pragma unroll
+                for (int b = 0; b < kLLBatch; b++)
+                    if (b < nbw) acc[b] = hop_word<DT, hop_op>(acc[b], (uint32_t)v[b]);
+            }
+            if (r == 0) {
+                if constexpr (OP == OP_AVG) {
+#pragma unroll
+                    for (int b = 0; b < kLLBatch; b++)
+                        if (b < nbw) acc[b] = scale_word<DT>(acc[b], a.inv_p);
+                }
+            } else {
+                // send the partial up, then wait for the final value
+                if (slow) ring_delay(a.fault_delay_ns);
+                unsigned long long *up = slot(parent, ls);
+#pragma unroll
+                for (int b = 0; b < kLLBatch; b++)
+                    if (b < nbw) st_relaxed_u64(up + w0 + b * GT, tag | acc[b]);
+                sent += (unsigned long long)elems;
+                const unsigned long long *in = slot(r, L);
+#pragma unroll
+                for (int b = 0; b < kLLBatch; b++)
+                    if (b < nbw) v[b] = ld_relaxed_u64(in + w0 + b * GT);
+                if (!ll_wait_batch(a, epoch, in, w0, GT, nbw, v, r, L, parent)) goto done;
+#pragma unroll
+                for (int b = 0; b < kLLBatch; b++)
+                    if (b < nbw) acc[b] = (uint32_t)v[b];
+            }
+            // broadcast: to the children, highest level first, then keep it
+            for (int l = ls - 1; l >= 0; l--) {
+                const int child = r + (1 << l);
+                if (child >= p) continue;
+                unsigned long long *down = slot(child, L);
+#pragma unroll
+                for (int b = 0; b < kLLBatch; b++)
+                    if (b < nbw) st_relaxed_u64(down + w0 + b * GT, tag | acc[b]);
+                sent += (unsigned long long)elems;
+            }
+#pragma unroll
+            for (int b = 0; b < kLLBatch; b++)
+                if (b < nbw) ll_store_word<DT>(own, (w0 + b * GT) * EPW, n, acc[b]);
+        }
+    }
+done:
+    atomicAdd(&s_sent, sent);
+    __syncthreads();
+    if (threadIdx.x == 0 && s_sent) atomicAdd(&a.recv_counts[r], s_sent);  // counted per sender
+    launch_epoch_end(a, epoch);
+}
+
 template <int DT, int OP>
 static cudaError_t launch_ll_t(const RingArgs &a, cudaStream_t stream) {
     void *args[] = {const_cast<RingArgs *>(&a)};
@@ -233,34 +341,74 @@ cudaError_t launch_ring_ll(const RingArgs &a, int dtype, int op, cudaStream_t st
 }
 
 template <int DT, int OP>
-static int ll_occ() {
+static cudaError_t launch_tree_ll_t(const RingArgs &a, cudaStream_t stream) {
+    void *args[] = {const_cast<RingArgs *>(&a)};
+    return cudaLaunchCooperativeKernel((const void *)tree_ll_kernel<DT, OP>, dim3((unsigned)(a.p * a.channels)),
+                                       dim3((unsigned)kLLThreads), args, 0, stream);
+}
+
+cudaError_t launch_tree_ll(const RingArgs &a, int dtype, int op, cudaStream_t stream) {
+    switch (dtype) {
+    case DT_I32:
+        if (op == OP_SUM) return launch_tree_ll_t<DT_I32, OP_SUM>(a, stream);
+        if (op == OP_MAX) return launch_tree_ll_t<DT_I32, OP_MAX>(a, stream);
+        break;
+    case DT_F32:
+        if (op == OP_SUM) return launch_tree_ll_t<DT_F32, OP_SUM>(a, stream);
+        if (op == OP_MAX) return launch_tree_ll_t<DT_F32, OP_MAX>(a, stream);
+        if (op == OP_AVG) return launch_tree_ll_t<DT_F32, OP_AVG>(a, stream);
+        break;
+    case DT_BF16:
+        if (op == OP_SUM) return launch_tree_ll_t<DT_BF16, OP_SUM>(a, stream);
+        if (op == OP_MAX) return launch_tree_ll_t<DT_BF16, OP_MAX>(a, stream);
+        if (op == OP_AVG) return launch_tree_ll_t<DT_BF16, OP_AVG>(a, stream);
+        break;
+    case DT_F16:
+        if (op == OP_SUM) return launch_tree_ll_t<DT_F16, OP_SUM>(a, stream);
+        if (op == OP_MAX) return launch_tree_ll_t<DT_F16, OP_MAX>(a, stream);
+        if (op == OP_AVG) return launch_tree_ll_t<DT_F16, OP_AVG>(a, stream);
+        break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename K>
+static int ll_occ_of(K kernel) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ring_ll_kernel<DT, OP>, kLLThreads, 0) != cudaSuccess)
-        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kLLThreads, 0) != cudaSuccess) return 0;
     return nb;
 }
 
-int ring_ll_max_coresident_ctas(int dtype, int op) {
+template <int DT, int OP>
+static int ll_occ(bool tree) {
+    if constexpr (OP == OP_AVG_PREDIV) {
+        return tree ? 0 : ll_occ_of(ring_ll_kernel<DT, OP>);
+    } else {
+        return tree ? ll_occ_of(tree_ll_kernel<DT, OP>) : ll_occ_of(ring_ll_kernel<DT, OP>);
+    }
+}
+
+int ll_max_coresident_ctas(bool tree, int dtype, int op) {
     int per_sm = 0;
     switch (dtype) {
-    case DT_I32: per_sm = op == OP_SUM ? ll_occ<DT_I32, OP_SUM>() : ll_occ<DT_I32, OP_MAX>(); break;
+    case DT_I32: per_sm = op == OP_SUM ? ll_occ<DT_I32, OP_SUM>(tree) : ll_occ<DT_I32, OP_MAX>(tree); break;
     case DT_F32:
-        per_sm = op == OP_SUM ? ll_occ<DT_F32, OP_SUM>()
-                 : op == OP_MAX ? ll_occ<DT_F32, OP_MAX>()
-                 : op == OP_AVG ? ll_occ<DT_F32, OP_AVG>()
-                                : ll_occ<DT_F32, OP_AVG_PREDIV>();
+        per_sm = op == OP_SUM ? ll_occ<DT_F32, OP_SUM>(tree)
+                 : op == OP_MAX ? ll_occ<DT_F32, OP_MAX>(tree)
+                 : op == OP_AVG ? ll_occ<DT_F32, OP_AVG>(tree)
+                                : ll_occ<DT_F32, OP_AVG_PREDIV>(tree);
         break;
     case DT_BF16:
-        per_sm = op == OP_SUM ? ll_occ<DT_BF16, OP_SUM>()
-                 : op == OP_MAX ? ll_occ<DT_BF16, OP_MAX>()
-                 : op == OP_AVG ? ll_occ<DT_BF16, OP_AVG>()
-                                : ll_occ<DT_BF16, OP_AVG_PREDIV>();
+        per_sm = op == OP_SUM ? ll_occ<DT_BF16, OP_SUM>(tree)
+                 : op == OP_MAX ? ll_occ<DT_BF16, OP_MAX>(tree)
+                 : op == OP_AVG ? ll_occ<DT_BF16, OP_AVG>(tree)
+                                : ll_occ<DT_BF16, OP_AVG_PREDIV>(tree);
         break;
     default:
-        per_sm = op == OP_SUM ? ll_occ<DT_F16, OP_SUM>()
-                 : op == OP_MAX ? ll_occ<DT_F16, OP_MAX>()
-                 : op == OP_AVG ? ll_occ<DT_F16, OP_AVG>()
-                                : ll_occ<DT_F16, OP_AVG_PREDIV>();
+        per_sm = op == OP_SUM ? ll_occ<DT_F16, OP_SUM>(tree)
+                 : op == OP_MAX ? ll_occ<DT_F16, OP_MAX>(tree)
+                 : op == OP_AVG ? ll_occ<DT_F16, OP_AVG>(tree)
+                                : ll_occ<DT_F16, OP_AVG_PREDIV>(tree);
         break;
     }
     int dev = 0, sms = 0;

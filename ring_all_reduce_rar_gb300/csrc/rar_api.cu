@@ -22,6 +22,13 @@ constexpr long long kLLMailboxWords = (long long)RAR_LL_MAILBOX_BYTES / 8;
 // protocol auto: the low-latency ring up to this many bytes per rank (p = 16
 // sweep on GB300: 31 us against 72 us at 4 KB per rank, 68 against 80 at 1 MB)
 constexpr size_t kLLAutoMaxBytes = (size_t)1 << 20;
+// protocol auto for the tree engine: from p = 16 (below that the
+// progress-word tree is as fast: its per-call cost is lower), up to this
+// many bytes per rank (p = 16: 20.5 us against 22.5 at 64 KB per rank,
+// 41 against 27 at 256 KB, where a thread carries several batches of words
+// through the whole tree one after the other)
+constexpr int kLLTreeAutoMinP = 16;
+constexpr size_t kLLTreeAutoMaxBytes = (size_t)64 << 10;
 
 thread_local std::string g_init_error;  // errors before a handle exists
 
@@ -181,12 +188,23 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long lo
             return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
     }
     const long long split = bidir ? n_total - n_total / 2 : n_total;  // chunk_bounds(n_total, 2)
-    const int fwd_channels = bidir ? (G + 1) / 2 : G;
-    const int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
+    int fwd_channels = bidir ? (G + 1) / 2 : G;
+    int min_g = bidir ? std::min(fwd_channels, G - fwd_channels) : G;
     // the longest chunk piece any ring of this launch moves
     const int rp = layout == RING_FLAT ? p : layout == RING_INTRA ? group : p / group;
     const long long seg = layout == RING_INTER ? (n_total + group - 1) / group : std::max(split, n_total - split);
     const long long maxchunk = std::min((seg + rp - 1) / rp, (long long)n);
+    // small buffers: no more channels than slices of at least 1024
+    // elements (an idle CTA still costs its launch and its finish count)
+    if (!h->opt.channels) {
+        const long long per_ring = std::max<long long>(1, (maxchunk + 1023) / 1024);
+        const long long needed = bidir ? 2 * per_ring : per_ring;
+        if (needed < G) {
+            G = (int)needed;
+            fwd_channels = bidir ? G / 2 : G;
+            min_g = bidir ? G / 2 : G;
+        }
+    }
     long long slice = h->opt.slice_elems;
     if (slice == 0) {
         slice = (maxchunk + min_g - 1) / min_g;
@@ -255,7 +273,7 @@ long long ll_slot_words(int p, size_t n, long long n_total, int dtype) {
 int launch_ring_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long long g_first, long long n_total,
                          int dtype, int op, long long slot_words, cudaStream_t stream) {
     const int threads = ring_ll_threads();
-    const int max_ctas = std::min(ring_ll_max_coresident_ctas(dtype, op), kMaxRingCtas);
+    const int max_ctas = std::min(ll_max_coresident_ctas(false, dtype, op), kMaxRingCtas);
     if (max_ctas < p) return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
     int G = h->opt.channels;
     if (G == 0) G = (int)std::min<long long>(max_ctas / p, (slot_words + threads - 1) / threads);
@@ -303,6 +321,72 @@ int launch_ring_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long
     return RAR_OK;
 }
 
+// Words per mailbox slot for the low-latency tree: the whole buffer, in
+// 32-bit words; 0 if p * (ceil(log2 p) + 1) such slots do not fit.
+long long tree_ll_slot_words(int p, size_t n, int dtype) {
+    int L = 0;
+    while ((1 << L) < p) L++;
+    const long long epw = 4 / elem_bytes(dtype);
+    const long long words = std::max<long long>(1, ((long long)n + epw - 1) / epw);
+    if ((long long)p * (L + 1) * words > kLLMailboxWords) return 0;
+    return words;
+}
+
+// The low-latency tree: one word per thread where the co-resident grid
+// allows it.
+int launch_tree_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dtype, int op, long long slot_words,
+                         cudaStream_t stream) {
+    const int threads = ring_ll_threads();
+    const int max_ctas = std::min(ll_max_coresident_ctas(true, dtype, op), kMaxRingCtas);
+    if (max_ctas < p) return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
+    int G = h->opt.channels;
+    if (G == 0) G = (int)std::min<long long>(max_ctas / p, (slot_words + threads - 1) / threads);
+    if ((long long)G * p > max_ctas) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
+    cudaError_t ce = cudaMemsetAsync(h->recv_counts, 0, sizeof(unsigned long long) * (size_t)p, stream);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the send counters");
+    RingArgs a;
+    a.bufs = ptrs;
+    a.n = (long long)n;
+    a.first = 0;
+    a.n_total = (long long)n;
+    a.p = p;
+    a.layout = TREE;
+    a.group = p;
+    a.channels = G;
+    a.fwd_channels = G;
+    a.split = (long long)n;
+    a.slice = 0;
+    a.first_step = 0;
+    a.n_steps = 0;
+    a.inv_p = 1.0f / (float)p;
+    a.epoch_word = h->epoch_words;
+    a.finish_count = h->epoch_words + 1;
+    a.flag_capacity = kMaxRingCtas;
+    a.flags = h->flags;
+    a.mailbox = h->ll_box;
+    a.mailbox_words = kLLMailboxWords;
+    a.slot_words = slot_words;
+    a.recv_counts = h->recv_counts;
+    a.status = h->status;
+    a.abort_word = h->abort_word;
+    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
+    a.fault_mode = h->opt.fault_mode;
+    a.fault_rank = h->opt.fault_rank;
+    a.fault_delay_ns = h->opt.fault_delay_ns;
+    ce = launch_tree_ll(a, dtype, op, stream);
+    if (ce != cudaSuccess) {
+        if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "tree grid cannot be co-resident");
+        return cuda_fail(h, ce, "launching the low-latency tree");
+    }
+    h->last_ring = true;
+    h->last_layout[0] = TREE;
+    h->last_channels[0] = G;
+    h->last_fwd_channels[0] = G;
+    h->last_group = p;
+    h->last_phases = 1;
+    return RAR_OK;
+}
+
 // The tree executor: every co-resident CTA, slices of about n / channels.
 int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dtype, int op, bool vec16,
                          cudaStream_t stream) {
@@ -315,6 +399,7 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
         G = max_ctas / p;
         if (G < 1) return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
     }
+    if (!h->opt.channels) G = (int)std::min<long long>(G, std::max<long long>(1, ((long long)n + 1023) / 1024));
     long long slice = h->opt.slice_elems;
     if (slice == 0) {
         slice = ((long long)n + G - 1) / G;
@@ -419,16 +504,20 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         }
         // data path: per-thread 128-bit loads ("registers") or the
         // rank-sequential bulk-copy streaming path.  Auto (measured on GB300):
-        // registers for p <= 16 below 256 MB over all ranks, streaming
-        // otherwise (p = 8 fp32: 0.90 against 0.88 at 25 MB per rank, 0.92
-        // against 0.95 at 48 MB; p = 16: tied at 16 MB per rank).
+        // streaming from 256 MB over all ranks and 8 MB per rank, registers
+        // below.  Registers / streaming, fraction of the roofline or time:
+        // p = 8 fp32, 25 MB per rank 0.90 / 0.88, 48 MB 0.92 / 0.95; p = 16,
+        // 16 MB per rank: tied; p = 64 bf16, 4 MB per rank 162 / 195 us,
+        // 8 MB 289 / 231 us.  Small buffers are latency-bound, and the
+        // streaming path walks the p ranks one bulk copy after another.
         const size_t bytes = n * (size_t)elem_bytes(dtype);
         const bool stream_ok = engine == RAR_ENGINE_FUSED && phase == PHASE_ALL && vec16;
         int path = h->opt.fused_path;
         if (path == 2 && !stream_ok)
             return fail(h, RAR_EUNSUPPORTED,
                         "the streaming path needs engine fused, a full all-reduce and 16-byte aligned rank buffers");
-        if (path == 0) path = (stream_ok && (p > 16 || (size_t)p * bytes >= (size_t)256 << 20)) ? 2 : 1;
+        if (path == 0)
+            path = (stream_ok && (size_t)p * bytes >= (size_t)256 << 20 && bytes >= (size_t)8 << 20) ? 2 : 1;
         if (path == 2) {
             // tile per rank: slice_elems, else the largest tile up to 32 KB
             // (a multiple of 512 bytes) that cuts the buffer into k rounds of
@@ -463,6 +552,16 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         RankPtrs ptrs;
         rc = fill_ptrs(h, ptrs, bufs, p, stream);
         if (rc != RAR_OK) return rc;
+        // hand-off protocol (rar_options.protocol), as for the ring
+        const int proto = h->opt.protocol;
+        if (proto != 1) {
+            const long long slot_words = tree_ll_slot_words(p, n, dtype);
+            if (proto == 2 && slot_words == 0)
+                return fail(h, RAR_EUNSUPPORTED, "the buffers are too large for the low-latency mailbox");
+            const bool fits = slot_words > 0 && ll_max_coresident_ctas(true, dtype, op) >= p;
+            if (proto == 2 || (fits && p >= kLLTreeAutoMinP && n * (size_t)elem_bytes(dtype) <= kLLTreeAutoMaxBytes))
+                return launch_tree_ll_phase(h, ptrs, p, n, dtype, op, slot_words, stream);
+        }
         return launch_tree_schedule(h, ptrs, p, n, dtype, op, vec16, stream);
     }
 
@@ -482,7 +581,8 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
             const long long slot_words = ll_slot_words(p, n, n_total, dtype);
             if (proto == 2 && slot_words == 0)
                 return fail(h, RAR_EUNSUPPORTED, "the buffers are too large for the low-latency mailbox");
-            if (slot_words > 0 && (proto == 2 || n * (size_t)elem_bytes(dtype) <= kLLAutoMaxBytes))
+            const bool fits = slot_words > 0 && ll_max_coresident_ctas(false, dtype, op) >= p;
+            if (proto == 2 || (fits && n * (size_t)elem_bytes(dtype) <= kLLAutoMaxBytes))
                 return launch_ring_ll_phase(h, ptrs, p, n, g_first, n_total, dtype, op, slot_words, stream);
         }
         const int first = phase == PHASE_AG ? p - 1 : 0;
@@ -724,6 +824,15 @@ int rar_send_counts(rar_handle h, unsigned long long *out, int p) {
 const char *rar_last_error(rar_handle h) {
     if (!h) return g_init_error.c_str();
     return h->err.c_str();
+}
+
+int rar_debug_set_epoch(rar_handle h, unsigned epoch) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    DeviceGuard dg(h->device);
+    cudaError_t ce = cudaDeviceSynchronize();
+    if (ce == cudaSuccess) ce = cudaMemcpy(h->epoch_words, &epoch, sizeof(unsigned), cudaMemcpyHostToDevice);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "setting the epoch");
+    return RAR_OK;
 }
 
 int rar_destroy(rar_handle h) {

@@ -94,7 +94,7 @@ struct RingArgs {
     unsigned *finish_count;
     int flag_capacity;                // progress words to clear when the epoch wraps
     unsigned long long *flags;        // [p * channels] progress words
-    // The low-latency ring's mailbox (ring_ll.cu): words tagged with the
+    // The low-latency mailbox (ll.cu): words tagged with the
     // launch's epoch, so any launch that wraps the epoch clears all of them;
     // slot_words = words per (rank, step) slot.  NULL / 0 where unused.
     unsigned long long *mailbox;
@@ -129,12 +129,15 @@ cudaError_t launch_tree(const RingArgs &a, int dtype, int op, bool vec16, int th
 int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads);
 // Largest co-resident grid for the ring kernel of this dtype/op (per device).
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
-// Low-latency ring (ring_ll.cu): full all-reduce on the flat forward ring,
-// p * channels CTAs of ring_ll_threads() threads; a.mailbox holds
+// Low-latency hand-offs (ll.cu), p * channels CTAs of ring_ll_threads()
+// threads.  Ring: full all-reduce on the flat forward ring; a.mailbox holds
 // p * 2 (p - 1) slots of a.slot_words words (at least the longest chunk
-// part, in 32-bit words).
+// part, in 32-bit words).  Tree: full all-reduce with sum, max or avg;
+// p * (ceil(log2 p) + 1) slots of at least the buffer's words; a.recv_counts
+// holds p per-sender counters, zeroed by the caller.
 cudaError_t launch_ring_ll(const RingArgs &a, int dtype, int op, cudaStream_t stream);
-int ring_ll_max_coresident_ctas(int dtype, int op);
+cudaError_t launch_tree_ll(const RingArgs &a, int dtype, int op, cudaStream_t stream);
+int ll_max_coresident_ctas(bool tree, int dtype, int op);
 int ring_ll_threads();
 
 }  // namespace rar

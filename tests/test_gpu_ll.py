@@ -1,30 +1,17 @@
-"""GPU: the ring engine's low-latency hand-off (rar_options.protocol).  It
-runs the schedule of "Ring All-Reduce, in depth", "The schedule" with every
-message word tagged by the launch, so its results and send counts must equal
-the oracle's ring exactly, like the progress-word executor's.  The parity
-cases shared with the other engines run it as "ring_ll" in
-test_gpu_parity.py; this file covers what is particular to it."""
+"""GPU: the low-latency hand-off (rar_options.protocol) of the ring and tree
+engines.  They run the schedules of "Ring All-Reduce, in depth", "The
+schedule" and of the tree in "Derive the cost of a ring all-reduce" with
+every message word tagged by the launch, so results and send counts must
+equal the oracle's exactly, like the progress-word executors'.  The parity
+cases shared with the other engines run them as "ring_ll" / "tree_ll" in
+test_gpu_parity.py; this file covers what is particular to them."""
 import pytest
 import torch
 
-import oracle
-import workloads as w
-from tests.test_gpu_parity import assert_bits_equal, dev, gen, oracle_expect, rar, run_case, upload  # noqa: F401
+from tests.test_gpu_parity import (MAILBOX_BYTES, assert_bits_equal, dev, gen, oracle_expect, rar,  # noqa: F401
+                                   run_case, upload)
 
 pytestmark = pytest.mark.gpu
-
-
-
-def _mailbox_bytes():
-    import os
-    import re
-    from tests.conftest import ROOT
-    text = open(os.path.join(ROOT, "include", "rar.h")).read()
-    m = re.search(r"#define RAR_LL_MAILBOX_BYTES \((\d+)u << (\d+)\)", text)
-    return int(m.group(1)) << int(m.group(2))
-
-
-MAILBOX_BYTES = _mailbox_bytes()
 
 
 def test_channel_counts_do_not_change_results(rar, dev):
@@ -149,3 +136,38 @@ def test_ranges_on_the_low_latency_ring(rar, dev):
     torch.cuda.synchronize()
     assert_bits_equal(rows, ref, "ranges")
     assert total == list(sends)
+
+
+def test_tree_channel_counts_do_not_change_results(rar, dev):
+    """Low-latency tree: with few channels a thread carries several batches
+    of words through the whole tree, one batch after the other."""
+    p, n = 13, 3000 * 13 + 7
+    host = gen(p, n, "float32", ("normal", 1.0), 51)
+    ref, _ = oracle_expect(host, "float32", "sum", "tree")
+    for ch in [1, 3, 50]:
+        _, rows = upload(host, dev)
+        with rar.Handle(0, engine="tree", protocol="ll", channels=ch) as h:
+            h.allreduce(rows)
+            h.check()
+            sends = h.send_counts(p)
+        assert_bits_equal(rows, ref, f"channels={ch}")
+        assert sum(sends) == 2 * (p - 1) * n
+
+
+def test_tree_mailbox_limit(rar, dev):
+    """The low-latency tree needs p * (ceil(log2 p) + 1) buffer-sized slots."""
+    p = 16
+    n_fit = MAILBOX_BYTES // (8 * p * 5)  # fp32: one element per word, 5 slots at p = 16
+    for n, ok in [(n_fit, True), (n_fit + 1, False)]:
+        host = gen(p, n, "float32", ("normal", 1.0), 57)
+        _, rows = upload(host, dev)
+        with rar.Handle(0, engine="tree", protocol="ll") as h:
+            if ok:
+                h.allreduce(rows)
+                h.check()
+                ref, _ = oracle_expect(host, "float32", "sum", "tree")
+                assert_bits_equal(rows, ref, f"n={n}")
+            else:
+                with pytest.raises(rar.RarError) as e:
+                    h.allreduce(rows)
+                assert e.value.code == 2

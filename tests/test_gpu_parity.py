@@ -20,12 +20,24 @@ RING_ENGINES = ["fused", "fused_regs", "fused_stream", "ring", "ring_bidir"]
 # streaming (bulk-copy) data path; "fused" lets the library choose.  "ring"
 # is the ring executor with progress words; "ring_ll" the same schedule with
 # the low-latency hand-off (tests/test_gpu_ll.py).
+def _mailbox_bytes():
+    import os
+    import re
+    from tests.conftest import ROOT
+    text = open(os.path.join(ROOT, "include", "rar.h")).read()
+    m = re.search(r"#define RAR_LL_MAILBOX_BYTES \((\d+)u << (\d+)\)", text)
+    return int(m.group(1)) << int(m.group(2))
+
+
+MAILBOX_BYTES = _mailbox_bytes()
 # small-buffer tests also run the low-latency ring
 SMALL_ENGINES = RING_ENGINES + ["ring_ll"]
 ENGINE_OPTS = {"fused_regs": dict(engine="fused", fused_path="registers"),
                "fused_stream": dict(engine="fused", fused_path="stream"),
                "ring": dict(engine="ring", protocol="simple"),
-               "ring_ll": dict(engine="ring", protocol="ll")}
+               "ring_ll": dict(engine="ring", protocol="ll"),
+               "tree": dict(engine="tree", protocol="simple"),
+               "tree_ll": dict(engine="tree", protocol="ll")}
 
 
 def handle_opts(engine, **opts):
@@ -65,7 +77,7 @@ def oracle_expect(host_rows, dtype, op, engine):
     ref = [w.to_storage_numpy(t).copy() for t in host_rows]
     if engine == "ring_bidir":
         sends = oracle.simulate_bidir(ref, dtype, op)
-    elif engine in ("fused_tree", "tree"):
+    elif engine in ("fused_tree", "tree", "tree_ll"):
         oracle.tree_fold(ref, dtype, op)
         sends = None
     else:
@@ -95,7 +107,7 @@ def run_case(rar, dev, host_rows, dtype, op, engine, offset=0, **opts):
     p, n = len(rows), rows[0].numel()
     if engine in ("ring", "ring_ll", "ring_bidir"):
         assert list(got_sends) == list(sends)
-    elif engine == "tree":
+    elif engine in ("tree", "tree_ll"):
         assert sum(got_sends) == 2 * (p - 1) * n
     else:
         assert list(got_sends) == [0] * p
@@ -296,11 +308,11 @@ def test_large_p_uses_pointer_table(rar, dev, engine):
     run_case(rar, dev, host, "float32", "sum", engine)
 
 
-@pytest.mark.parametrize("engine", ["fused_regs", "fused_stream", "fused_tree", "tree"])
+@pytest.mark.parametrize("engine", ["fused_regs", "fused_stream", "fused_tree", "tree", "tree_ll"])
 def test_largest_p(rar, dev, engine):
     """p at the top of the range: 1024 ranks (the fused engines: pointer
-    table, runtime p); 200 ranks for the tree executor (one CTA per rank)."""
-    p = 200 if engine == "tree" else 1024
+    table, runtime p); 200 ranks for the tree executors (one CTA per rank)."""
+    p = 200 if engine in ("tree", "tree_ll") else 1024
     host = gen(p, 2 * p + 37, "float32", ("normal", 1.0), 13)
     run_case(rar, dev, host, "float32", "sum", engine)
 
@@ -392,6 +404,24 @@ def test_ring_muted_rank_times_out_and_handle_recovers(rar, dev, engine):
         h.allreduce(rows)
         h.check()
         assert_bits_equal(rows, ref, "after timeout")
+
+
+@pytest.mark.parametrize("engine", ["ring", "ring_ll", "ring_bidir", "tree", "tree_ll"])
+def test_epoch_wrap_around(rar, dev, engine):
+    """Progress and mailbox words carry a 32-bit launch epoch.  The launch
+    that runs with epoch 0xFFFFFFFF clears them and restarts the count, so
+    calls on either side of the wrap stay exact (without the clearing, the
+    old high tags would satisfy every wait after the wrap)."""
+    host = gen(8, 8 * 3000 + 5, "bfloat16", ("normal", 1e-2), 90)
+    ref, _ = oracle_expect(host, "bfloat16", "sum", engine)
+    with rar.Handle(0, **handle_opts(engine)) as h:
+        for start, calls in [(0xFFFFFFF0, 2), (0xFFFFFFFD, 5)]:
+            rar.rar_debug_set_epoch(h.h, start)
+            for k in range(calls):
+                _, rows = upload(host, dev)
+                h.allreduce(rows)
+                h.check()
+                assert_bits_equal(rows, ref, f"{engine}: epoch {start + k + 1:#x}")
 
 
 def test_ring_straggler_keeps_results(rar, dev):
@@ -514,20 +544,26 @@ def _tree_children(r, p):
     return kids
 
 
+@pytest.mark.parametrize("protocol", ["simple", "ll"])
 @pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "sum"), ("float16", "avg"),
                                       ("float32", "max"), ("int32", "sum"), ("bfloat16", "avg")])
-def test_tree_executor_matches_tree_order(rar, dev, dtype, op):
+def test_tree_executor_matches_tree_order(rar, dev, dtype, op, protocol):
     """"Derive the cost of a ring all-reduce": reduce up a binary tree,
     broadcast down.  The executor folds in the oracle's tree order bit for
-    bit; every non-root rank sends n up once and n to each child."""
+    bit, with either hand-off; every non-root rank sends n up once and n to
+    each child."""
     dist = ("uniform_int", -(1 << 20), 21) if dtype == "int32" else ("normal", 1.0)
+    e = 2 if dtype in ("bfloat16", "float16") else 4
     for p in [2, 3, 4, 5, 7, 8, 13, 16, 64]:
         for n in [1, p + 3, 4099, 64 * 1000 + 5]:
+            levels = max(1, (p - 1).bit_length())
+            if protocol == "ll" and p * (levels + 1) * -(-n * e // 4) * 8 > MAILBOX_BYTES:
+                continue  # does not fit the low-latency mailbox
             host = gen(p, n, dtype, dist, 300 + p * 7 + n)
             ref = [w.to_storage_numpy(t).copy() for t in host]
             oracle.tree_fold(ref, dtype, op)
             _, rows = upload(host, dev)
-            with rar.Handle(0, engine="tree") as h:
+            with rar.Handle(0, engine="tree", protocol=protocol) as h:
                 h.allreduce(rows, op=op)
                 h.check()
                 sends = h.send_counts(p)
@@ -538,10 +574,12 @@ def test_tree_executor_matches_tree_order(rar, dev, dtype, op):
             assert sum(sends) == 2 * (p - 1) * n
 
 
-def test_tree_executor_fault_and_rejections(rar, dev):
+@pytest.mark.parametrize("protocol", ["simple", "ll"])
+def test_tree_executor_fault_and_rejections(rar, dev, protocol):
     host = gen(8, 8 * 4096, "float32", ("normal", 1.0), 8)
     _, rows = upload(host, dev)
-    with rar.Handle(0, engine="tree", timeout_ns=50_000_000, fault_mode="mute", fault_rank=2) as h:
+    with rar.Handle(0, engine="tree", protocol=protocol, timeout_ns=50_000_000, fault_mode="mute",
+                    fault_rank=2) as h:
         # rank 2 is waited on by rank 0 at level 1 (a muted leaf such as rank 1
         # stalls nobody: its data is only read at step 0, which has no wait)
         h.allreduce(rows)
@@ -560,8 +598,8 @@ def test_tree_executor_fault_and_rejections(rar, dev):
 # ----------------------------------------------------------------- CUDA graphs
 
 @pytest.mark.parametrize("engine,opts", [("fused_regs", {}), ("fused_stream", {}), ("ring", {}), ("ring_ll", {}),
-                                         ("ring_bidir", {}), ("tree", {}), ("ring", dict(hier_group=2)),
-                                         ("fused_tree", {})])
+                                         ("ring_bidir", {}), ("tree", {}), ("tree_ll", {}),
+                                         ("ring", dict(hier_group=2)), ("fused_tree", {})])
 def test_captured_call_replays(rar, dev, engine, opts):
     """A call recorded with stream capture replays correctly again and again:
     the ring and tree executors take their epoch from device memory."""

@@ -12,9 +12,41 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "rar_internal.h"
 
 namespace rar {
+
+template <int V>
+using IntC = std::integral_constant<int, V>;
+
+// Runtime (dtype, op) to a kernel instantiation: calls
+// f(IntC<dtype>{}, IntC<op>{}) for every pair the library offers -- sum and
+// max on every dtype, avg on the floating types, avg_prediv on the floating
+// types where kPrediv -- and returns `none` for any other pair.
+template <bool kPrediv, typename R, typename F>
+R dispatch_dtype_op(int dtype, int op, R none, F &&f) {
+    auto floating = [&](auto dt) -> R {
+        if (op == OP_SUM) return f(dt, IntC<OP_SUM>{});
+        if (op == OP_MAX) return f(dt, IntC<OP_MAX>{});
+        if (op == OP_AVG) return f(dt, IntC<OP_AVG>{});
+        if constexpr (kPrediv) {
+            if (op == OP_AVG_PREDIV) return f(dt, IntC<OP_AVG_PREDIV>{});
+        }
+        return none;
+    };
+    switch (dtype) {
+    case DT_I32:
+        if (op == OP_SUM) return f(IntC<DT_I32>{}, IntC<OP_SUM>{});
+        if (op == OP_MAX) return f(IntC<DT_I32>{}, IntC<OP_MAX>{});
+        return none;
+    case DT_F32: return floating(IntC<DT_F32>{});
+    case DT_BF16: return floating(IntC<DT_BF16>{});
+    case DT_F16: return floating(IntC<DT_F16>{});
+    }
+    return none;
+}
 
 template <int DT> struct ElemInfo;
 template <> struct ElemInfo<DT_I32> { static constexpr int bytes = 4; };

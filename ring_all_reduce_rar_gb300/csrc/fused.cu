@@ -6,31 +6,9 @@ namespace rar {
 
 cudaError_t launch_fused(const FusedArgs &a, int dtype, int op, bool tree, bool vec16, int threads,
                          cudaStream_t stream) {
-    switch (dtype) {
-    case DT_I32:
-        if (op == OP_SUM) return launch_fused_op<DT_I32, OP_SUM>(a, tree, vec16, threads, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_I32, OP_MAX>(a, tree, vec16, threads, stream);
-        break;
-    case DT_F32:
-        if (op == OP_SUM) return launch_fused_op<DT_F32, OP_SUM>(a, tree, vec16, threads, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_F32, OP_MAX>(a, tree, vec16, threads, stream);
-        if (op == OP_AVG) return launch_fused_op<DT_F32, OP_AVG>(a, tree, vec16, threads, stream);
-        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_F32, OP_AVG_PREDIV>(a, tree, vec16, threads, stream);
-        break;
-    case DT_BF16:
-        if (op == OP_SUM) return launch_fused_op<DT_BF16, OP_SUM>(a, tree, vec16, threads, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_BF16, OP_MAX>(a, tree, vec16, threads, stream);
-        if (op == OP_AVG) return launch_fused_op<DT_BF16, OP_AVG>(a, tree, vec16, threads, stream);
-        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_BF16, OP_AVG_PREDIV>(a, tree, vec16, threads, stream);
-        break;
-    case DT_F16:
-        if (op == OP_SUM) return launch_fused_op<DT_F16, OP_SUM>(a, tree, vec16, threads, stream);
-        if (op == OP_MAX) return launch_fused_op<DT_F16, OP_MAX>(a, tree, vec16, threads, stream);
-        if (op == OP_AVG) return launch_fused_op<DT_F16, OP_AVG>(a, tree, vec16, threads, stream);
-        if (op == OP_AVG_PREDIV) return launch_fused_op<DT_F16, OP_AVG_PREDIV>(a, tree, vec16, threads, stream);
-        break;
-    }
-    return cudaErrorInvalidValue;
+    return dispatch_dtype_op<true>(dtype, op, cudaErrorInvalidValue, [&](auto dt, auto o) {
+        return launch_fused_op<decltype(dt)::value, decltype(o)::value>(a, tree, vec16, threads, stream);
+    });
 }
 
 template <int DT, int OP>
@@ -50,31 +28,9 @@ static cudaError_t launch_hier_t(const FusedArgs &a, int g, bool vec16, int thre
 
 cudaError_t launch_fused_hier(const FusedArgs &a, int dtype, int op, int g, bool vec16, int threads,
                               cudaStream_t stream) {
-    switch (dtype) {
-    case DT_I32:
-        if (op == OP_SUM) return launch_hier_t<DT_I32, OP_SUM>(a, g, vec16, threads, stream);
-        if (op == OP_MAX) return launch_hier_t<DT_I32, OP_MAX>(a, g, vec16, threads, stream);
-        break;
-    case DT_F32:
-        if (op == OP_SUM) return launch_hier_t<DT_F32, OP_SUM>(a, g, vec16, threads, stream);
-        if (op == OP_MAX) return launch_hier_t<DT_F32, OP_MAX>(a, g, vec16, threads, stream);
-        if (op == OP_AVG) return launch_hier_t<DT_F32, OP_AVG>(a, g, vec16, threads, stream);
-        if (op == OP_AVG_PREDIV) return launch_hier_t<DT_F32, OP_AVG_PREDIV>(a, g, vec16, threads, stream);
-        break;
-    case DT_BF16:
-        if (op == OP_SUM) return launch_hier_t<DT_BF16, OP_SUM>(a, g, vec16, threads, stream);
-        if (op == OP_MAX) return launch_hier_t<DT_BF16, OP_MAX>(a, g, vec16, threads, stream);
-        if (op == OP_AVG) return launch_hier_t<DT_BF16, OP_AVG>(a, g, vec16, threads, stream);
-        if (op == OP_AVG_PREDIV) return launch_hier_t<DT_BF16, OP_AVG_PREDIV>(a, g, vec16, threads, stream);
-        break;
-    case DT_F16:
-        if (op == OP_SUM) return launch_hier_t<DT_F16, OP_SUM>(a, g, vec16, threads, stream);
-        if (op == OP_MAX) return launch_hier_t<DT_F16, OP_MAX>(a, g, vec16, threads, stream);
-        if (op == OP_AVG) return launch_hier_t<DT_F16, OP_AVG>(a, g, vec16, threads, stream);
-        if (op == OP_AVG_PREDIV) return launch_hier_t<DT_F16, OP_AVG_PREDIV>(a, g, vec16, threads, stream);
-        break;
-    }
-    return cudaErrorInvalidValue;
+    return dispatch_dtype_op<true>(dtype, op, cudaErrorInvalidValue, [&](auto dt, auto o) {
+        return launch_hier_t<decltype(dt)::value, decltype(o)::value>(a, g, vec16, threads, stream);
+    });
 }
 
 }  // namespace rar

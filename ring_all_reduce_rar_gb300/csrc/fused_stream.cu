@@ -357,31 +357,9 @@ cudaError_t launch_fused_stream(const FusedArgs &a, int dtype, int op, int tile_
         return cudaErrorInvalidValue;
     if (n_stages < 2 || n_stages > kStreamMaxStages || (size_t)(n_stages + 2) * tile_bytes > 227 * 1024)
         return cudaErrorInvalidValue;
-    switch (dtype) {
-    case DT_I32:
-        if (op == OP_SUM) return launch_stream_t<DT_I32, OP_SUM>(a, tile_bytes, n_stages, stream);
-        if (op == OP_MAX) return launch_stream_t<DT_I32, OP_MAX>(a, tile_bytes, n_stages, stream);
-        break;
-    case DT_F32:
-        if (op == OP_SUM) return launch_stream_t<DT_F32, OP_SUM>(a, tile_bytes, n_stages, stream);
-        if (op == OP_MAX) return launch_stream_t<DT_F32, OP_MAX>(a, tile_bytes, n_stages, stream);
-        if (op == OP_AVG) return launch_stream_t<DT_F32, OP_AVG>(a, tile_bytes, n_stages, stream);
-        if (op == OP_AVG_PREDIV) return launch_stream_t<DT_F32, OP_AVG_PREDIV>(a, tile_bytes, n_stages, stream);
-        break;
-    case DT_BF16:
-        if (op == OP_SUM) return launch_stream_t<DT_BF16, OP_SUM>(a, tile_bytes, n_stages, stream);
-        if (op == OP_MAX) return launch_stream_t<DT_BF16, OP_MAX>(a, tile_bytes, n_stages, stream);
-        if (op == OP_AVG) return launch_stream_t<DT_BF16, OP_AVG>(a, tile_bytes, n_stages, stream);
-        if (op == OP_AVG_PREDIV) return launch_stream_t<DT_BF16, OP_AVG_PREDIV>(a, tile_bytes, n_stages, stream);
-        break;
-    case DT_F16:
-        if (op == OP_SUM) return launch_stream_t<DT_F16, OP_SUM>(a, tile_bytes, n_stages, stream);
-        if (op == OP_MAX) return launch_stream_t<DT_F16, OP_MAX>(a, tile_bytes, n_stages, stream);
-        if (op == OP_AVG) return launch_stream_t<DT_F16, OP_AVG>(a, tile_bytes, n_stages, stream);
-        if (op == OP_AVG_PREDIV) return launch_stream_t<DT_F16, OP_AVG_PREDIV>(a, tile_bytes, n_stages, stream);
-        break;
-    }
-    return cudaErrorInvalidValue;
+    return dispatch_dtype_op<true>(dtype, op, cudaErrorInvalidValue, [&](auto dt, auto o) {
+        return launch_stream_t<decltype(dt)::value, decltype(o)::value>(a, tile_bytes, n_stages, stream);
+    });
 }
 
 }  // namespace rar

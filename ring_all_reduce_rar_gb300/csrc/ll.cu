@@ -313,31 +313,9 @@ static cudaError_t launch_ll_t(const RingArgs &a, cudaStream_t stream) {
 }
 
 cudaError_t launch_ring_ll(const RingArgs &a, int dtype, int op, cudaStream_t stream) {
-    switch (dtype) {
-    case DT_I32:
-        if (op == OP_SUM) return launch_ll_t<DT_I32, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_ll_t<DT_I32, OP_MAX>(a, stream);
-        break;
-    case DT_F32:
-        if (op == OP_SUM) return launch_ll_t<DT_F32, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_ll_t<DT_F32, OP_MAX>(a, stream);
-        if (op == OP_AVG) return launch_ll_t<DT_F32, OP_AVG>(a, stream);
-        if (op == OP_AVG_PREDIV) return launch_ll_t<DT_F32, OP_AVG_PREDIV>(a, stream);
-        break;
-    case DT_BF16:
-        if (op == OP_SUM) return launch_ll_t<DT_BF16, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_ll_t<DT_BF16, OP_MAX>(a, stream);
-        if (op == OP_AVG) return launch_ll_t<DT_BF16, OP_AVG>(a, stream);
-        if (op == OP_AVG_PREDIV) return launch_ll_t<DT_BF16, OP_AVG_PREDIV>(a, stream);
-        break;
-    case DT_F16:
-        if (op == OP_SUM) return launch_ll_t<DT_F16, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_ll_t<DT_F16, OP_MAX>(a, stream);
-        if (op == OP_AVG) return launch_ll_t<DT_F16, OP_AVG>(a, stream);
-        if (op == OP_AVG_PREDIV) return launch_ll_t<DT_F16, OP_AVG_PREDIV>(a, stream);
-        break;
-    }
-    return cudaErrorInvalidValue;
+    return dispatch_dtype_op<true>(dtype, op, cudaErrorInvalidValue, [&](auto dt, auto o) {
+        return launch_ll_t<decltype(dt)::value, decltype(o)::value>(a, stream);
+    });
 }
 
 template <int DT, int OP>
@@ -348,28 +326,9 @@ static cudaError_t launch_tree_ll_t(const RingArgs &a, cudaStream_t stream) {
 }
 
 cudaError_t launch_tree_ll(const RingArgs &a, int dtype, int op, cudaStream_t stream) {
-    switch (dtype) {
-    case DT_I32:
-        if (op == OP_SUM) return launch_tree_ll_t<DT_I32, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_tree_ll_t<DT_I32, OP_MAX>(a, stream);
-        break;
-    case DT_F32:
-        if (op == OP_SUM) return launch_tree_ll_t<DT_F32, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_tree_ll_t<DT_F32, OP_MAX>(a, stream);
-        if (op == OP_AVG) return launch_tree_ll_t<DT_F32, OP_AVG>(a, stream);
-        break;
-    case DT_BF16:
-        if (op == OP_SUM) return launch_tree_ll_t<DT_BF16, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_tree_ll_t<DT_BF16, OP_MAX>(a, stream);
-        if (op == OP_AVG) return launch_tree_ll_t<DT_BF16, OP_AVG>(a, stream);
-        break;
-    case DT_F16:
-        if (op == OP_SUM) return launch_tree_ll_t<DT_F16, OP_SUM>(a, stream);
-        if (op == OP_MAX) return launch_tree_ll_t<DT_F16, OP_MAX>(a, stream);
-        if (op == OP_AVG) return launch_tree_ll_t<DT_F16, OP_AVG>(a, stream);
-        break;
-    }
-    return cudaErrorInvalidValue;
+    return dispatch_dtype_op<false>(dtype, op, cudaErrorInvalidValue, [&](auto dt, auto o) {
+        return launch_tree_ll_t<decltype(dt)::value, decltype(o)::value>(a, stream);
+    });
 }
 
 template <typename K>
@@ -379,38 +338,14 @@ static int ll_occ_of(K kernel) {
     return nb;
 }
 
-template <int DT, int OP>
-static int ll_occ(bool tree) {
-    if constexpr (OP == OP_AVG_PREDIV) {
-        return tree ? 0 : ll_occ_of(ring_ll_kernel<DT, OP>);
-    } else {
-        return tree ? ll_occ_of(tree_ll_kernel<DT, OP>) : ll_occ_of(ring_ll_kernel<DT, OP>);
-    }
-}
-
 int ll_max_coresident_ctas(bool tree, int dtype, int op) {
-    int per_sm = 0;
-    switch (dtype) {
-    case DT_I32: per_sm = op == OP_SUM ? ll_occ<DT_I32, OP_SUM>(tree) : ll_occ<DT_I32, OP_MAX>(tree); break;
-    case DT_F32:
-        per_sm = op == OP_SUM ? ll_occ<DT_F32, OP_SUM>(tree)
-                 : op == OP_MAX ? ll_occ<DT_F32, OP_MAX>(tree)
-                 : op == OP_AVG ? ll_occ<DT_F32, OP_AVG>(tree)
-                                : ll_occ<DT_F32, OP_AVG_PREDIV>(tree);
-        break;
-    case DT_BF16:
-        per_sm = op == OP_SUM ? ll_occ<DT_BF16, OP_SUM>(tree)
-                 : op == OP_MAX ? ll_occ<DT_BF16, OP_MAX>(tree)
-                 : op == OP_AVG ? ll_occ<DT_BF16, OP_AVG>(tree)
-                                : ll_occ<DT_BF16, OP_AVG_PREDIV>(tree);
-        break;
-    default:
-        per_sm = op == OP_SUM ? ll_occ<DT_F16, OP_SUM>(tree)
-                 : op == OP_MAX ? ll_occ<DT_F16, OP_MAX>(tree)
-                 : op == OP_AVG ? ll_occ<DT_F16, OP_AVG>(tree)
-                                : ll_occ<DT_F16, OP_AVG_PREDIV>(tree);
-        break;
-    }
+    const int per_sm =
+        tree ? dispatch_dtype_op<false>(dtype, op, 0, [&](auto dt, auto o) {
+                   return ll_occ_of(tree_ll_kernel<decltype(dt)::value, decltype(o)::value>);
+               })
+             : dispatch_dtype_op<true>(dtype, op, 0, [&](auto dt, auto o) {
+                   return ll_occ_of(ring_ll_kernel<decltype(dt)::value, decltype(o)::value>);
+               });
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -132,28 +132,9 @@ static cudaError_t launch_tree_op(const RingArgs &a, bool vec16, int threads, cu
 }
 
 cudaError_t launch_tree(const RingArgs &a, int dtype, int op, bool vec16, int threads, cudaStream_t stream) {
-    switch (dtype) {
-    case DT_I32:
-        if (op == OP_SUM) return launch_tree_op<DT_I32, OP_SUM>(a, vec16, threads, stream);
-        if (op == OP_MAX) return launch_tree_op<DT_I32, OP_MAX>(a, vec16, threads, stream);
-        break;
-    case DT_F32:
-        if (op == OP_SUM) return launch_tree_op<DT_F32, OP_SUM>(a, vec16, threads, stream);
-        if (op == OP_MAX) return launch_tree_op<DT_F32, OP_MAX>(a, vec16, threads, stream);
-        if (op == OP_AVG) return launch_tree_op<DT_F32, OP_AVG>(a, vec16, threads, stream);
-        break;
-    case DT_BF16:
-        if (op == OP_SUM) return launch_tree_op<DT_BF16, OP_SUM>(a, vec16, threads, stream);
-        if (op == OP_MAX) return launch_tree_op<DT_BF16, OP_MAX>(a, vec16, threads, stream);
-        if (op == OP_AVG) return launch_tree_op<DT_BF16, OP_AVG>(a, vec16, threads, stream);
-        break;
-    case DT_F16:
-        if (op == OP_SUM) return launch_tree_op<DT_F16, OP_SUM>(a, vec16, threads, stream);
-        if (op == OP_MAX) return launch_tree_op<DT_F16, OP_MAX>(a, vec16, threads, stream);
-        if (op == OP_AVG) return launch_tree_op<DT_F16, OP_AVG>(a, vec16, threads, stream);
-        break;
-    }
-    return cudaErrorInvalidValue;
+    return dispatch_dtype_op<false>(dtype, op, cudaErrorInvalidValue, [&](auto dt, auto o) {
+        return launch_tree_op<decltype(dt)::value, decltype(o)::value>(a, vec16, threads, stream);
+    });
 }
 
 template <typename K>
@@ -170,25 +151,9 @@ static int tree_occ(bool vec16, int threads) {
 }
 
 int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads) {
-    int per_sm = 0;
-    switch (dtype) {
-    case DT_I32: per_sm = op == OP_SUM ? tree_occ<DT_I32, OP_SUM>(vec16, threads) : tree_occ<DT_I32, OP_MAX>(vec16, threads); break;
-    case DT_F32:
-        per_sm = op == OP_SUM ? tree_occ<DT_F32, OP_SUM>(vec16, threads)
-                 : op == OP_MAX ? tree_occ<DT_F32, OP_MAX>(vec16, threads)
-                                : tree_occ<DT_F32, OP_AVG>(vec16, threads);
-        break;
-    case DT_BF16:
-        per_sm = op == OP_SUM ? tree_occ<DT_BF16, OP_SUM>(vec16, threads)
-                 : op == OP_MAX ? tree_occ<DT_BF16, OP_MAX>(vec16, threads)
-                                : tree_occ<DT_BF16, OP_AVG>(vec16, threads);
-        break;
-    default:
-        per_sm = op == OP_SUM ? tree_occ<DT_F16, OP_SUM>(vec16, threads)
-                 : op == OP_MAX ? tree_occ<DT_F16, OP_MAX>(vec16, threads)
-                                : tree_occ<DT_F16, OP_AVG>(vec16, threads);
-        break;
-    }
+    const int per_sm = dispatch_dtype_op<false>(dtype, op, 0, [&](auto dt, auto o) {
+        return tree_occ<decltype(dt)::value, decltype(o)::value>(vec16, threads);
+    });
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

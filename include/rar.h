@@ -29,7 +29,9 @@
  *   RAR_ENGINE_RING        persistent executor: CTA groups play the ranks and
  *                          run the schedule step by step, slice-pipelined,
  *                          handing slices to the right neighbour through
- *                          acquire/release flags (5 (p - 1) n element moves);
+ *                          acquire/release flags (5 (p - 1) n element moves),
+ *                          or, for small buffers, through tagged words in a
+ *                          mailbox (rar_options.protocol);
  *   RAR_ENGINE_RING_BIDIR  as RING, with the buffer's second half run by a
  *                          ring in the opposite direction ("Bidirectional
  *                          rings" in "Ring All-Reduce, in depth", section
@@ -41,7 +43,8 @@
  *                          ("Derive the cost of a ring all-reduce": reduce up a
  *                          binary tree, broadcast down, 2 ceil(log2 p) steps);
  *                          same arithmetic as RAR_ENGINE_FUSED_TREE; full
- *                          all-reduce with sum, max or avg.
+ *                          all-reduce with sum, max or avg; the same two
+ *                          hand-offs as RAR_ENGINE_RING.
  *
  * Conventions for every call:
  *   - Return value: RAR_OK or a rar_status_code; rar_last_error(h) gives a
@@ -57,6 +60,11 @@
  *     legacy default stream) and the call returns without waiting.  One call
  *     in flight per handle: calls on one stream are ordered; calls on several
  *     streams with one handle must be ordered by the caller.
+ *   - Ring and tree engines run one cooperative launch of up to every
+ *     co-resident CTA of the device; the GPU runs all CTAs of a launch
+ *     together, and every wait inside is bounded (rar_options.timeout_ns),
+ *     so a launch that cannot make progress ends with RAR_ETIMEOUT rather
+ *     than hanging.
  *   - CUDA graphs: rar_allreduce, rar_reduce_scatter and rar_all_gather may
  *     be recorded with stream capture and replayed any number of times; the
  *     ring and tree executors keep their epoch in device memory, so every

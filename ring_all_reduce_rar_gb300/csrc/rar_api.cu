@@ -164,6 +164,55 @@ bool all_aligned16(void *const *bufs, int p) {
     return true;
 }
 
+// Record a ring or tree launch of the current call, for rar_send_counts:
+// launch `idx` of the call (the hierarchical schedule makes three).
+void note_ring_launch(rar_ctx *h, int idx, int layout, int channels, int fwd_channels, int group) {
+    h->last_ring = true;
+    h->last_layout[idx] = layout;
+    h->last_channels[idx] = channels;
+    h->last_fwd_channels[idx] = fwd_channels;
+    h->last_group = group;
+    h->last_phases = idx + 1;
+}
+
+// Launch arguments shared by every ring and tree launch of a handle: the
+// rank pointers, sizes, the handle's scratch (epoch, progress words,
+// mailbox, counters, status) and its timeout and fault options.  The caller
+// sets the schedule fields (layout, channels, slices, steps).
+RingArgs handle_ring_args(const rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long long g_first,
+                          long long n_total) {
+    RingArgs a;
+    a.bufs = ptrs;
+    a.n = (long long)n;
+    a.first = g_first;
+    a.n_total = n_total;
+    a.p = p;
+    a.layout = RING_FLAT;
+    a.group = p;
+    a.channels = 1;
+    a.fwd_channels = 1;
+    a.split = n_total;
+    a.slice = 0;
+    a.first_step = 0;
+    a.n_steps = 0;
+    a.inv_p = 1.0f / (float)p;
+    a.epoch_word = h->epoch_words;
+    a.finish_count = h->epoch_words + 1;
+    a.flag_capacity = kMaxRingCtas;
+    a.flags = h->flags;
+    a.mailbox = h->ll_box;
+    a.mailbox_words = kLLMailboxWords;
+    a.slot_words = 0;
+    a.recv_counts = h->recv_counts;
+    a.status = h->status;
+    a.abort_word = h->abort_word;
+    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
+    a.fault_mode = h->opt.fault_mode;
+    a.fault_rank = h->opt.fault_rank;
+    a.fault_delay_ns = h->opt.fault_delay_ns;
+    return a;
+}
+
 // One ring launch: `layout` picks the rings (flat; inside nodes of `group`;
 // across nodes), steps [first, first + steps) of that ring size, counters in
 // array `phase_idx`.  Channels and slices follow the tuned defaults unless
@@ -214,12 +263,7 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long lo
     slice = std::max<long long>(16, (slice + 15) / 16 * 16);
     while ((maxchunk + slice - 1) / slice / min_g > kMaxSlicesPerChannelStep) slice *= 2;
 
-    RingArgs a;
-    a.bufs = ptrs;
-    a.n = (long long)n;
-    a.first = g_first;
-    a.n_total = n_total;
-    a.p = p;
+    RingArgs a = handle_ring_args(h, ptrs, p, n, g_first, n_total);
     a.layout = layout;
     a.group = group;
     a.channels = G;
@@ -228,32 +272,13 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long lo
     a.slice = slice;
     a.first_step = first;
     a.n_steps = steps;
-    a.inv_p = 1.0f / (float)p;
-    a.epoch_word = h->epoch_words;
-    a.finish_count = h->epoch_words + 1;
-    a.flag_capacity = kMaxRingCtas;
-    a.flags = h->flags;
-    a.mailbox = h->ll_box;
-    a.mailbox_words = kLLMailboxWords;
-    a.slot_words = 0;
     a.recv_counts = h->recv_counts + (size_t)phase_idx * kMaxRingCtas;
-    a.status = h->status;
-    a.abort_word = h->abort_word;
-    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
-    a.fault_mode = h->opt.fault_mode;
-    a.fault_rank = h->opt.fault_rank;
-    a.fault_delay_ns = h->opt.fault_delay_ns;
     cudaError_t ce = launch_ring(a, dtype, op, vec16, threads, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "ring grid cannot be co-resident");
         return cuda_fail(h, ce, "launching the ring executor");
     }
-    h->last_ring = true;
-    h->last_layout[phase_idx] = layout;
-    h->last_channels[phase_idx] = G;
-    h->last_fwd_channels[phase_idx] = fwd_channels;
-    h->last_group = group;
-    h->last_phases = phase_idx + 1;
+    note_ring_launch(h, phase_idx, layout, G, fwd_channels, group);
     return RAR_OK;
 }
 
@@ -278,46 +303,17 @@ int launch_ring_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long
     int G = h->opt.channels;
     if (G == 0) G = (int)std::min<long long>(max_ctas / p, (slot_words + threads - 1) / threads);
     if ((long long)G * p > max_ctas) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
-    RingArgs a;
-    a.bufs = ptrs;
-    a.n = (long long)n;
-    a.first = g_first;
-    a.n_total = n_total;
-    a.p = p;
-    a.layout = RING_FLAT;
-    a.group = p;
+    RingArgs a = handle_ring_args(h, ptrs, p, n, g_first, n_total);
     a.channels = G;
     a.fwd_channels = G;
-    a.split = n_total;
-    a.slice = 0;
-    a.first_step = 0;
     a.n_steps = 2 * (p - 1);
-    a.inv_p = 1.0f / (float)p;
-    a.epoch_word = h->epoch_words;
-    a.finish_count = h->epoch_words + 1;
-    a.flag_capacity = kMaxRingCtas;
-    a.flags = h->flags;
-    a.mailbox = h->ll_box;
-    a.mailbox_words = kLLMailboxWords;
     a.slot_words = slot_words;
-    a.recv_counts = h->recv_counts;
-    a.status = h->status;
-    a.abort_word = h->abort_word;
-    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
-    a.fault_mode = h->opt.fault_mode;
-    a.fault_rank = h->opt.fault_rank;
-    a.fault_delay_ns = h->opt.fault_delay_ns;
     cudaError_t ce = launch_ring_ll(a, dtype, op, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "ring grid cannot be co-resident");
         return cuda_fail(h, ce, "launching the low-latency ring");
     }
-    h->last_ring = true;
-    h->last_layout[0] = RING_FLAT;
-    h->last_channels[0] = G;
-    h->last_fwd_channels[0] = G;
-    h->last_group = p;
-    h->last_phases = 1;
+    note_ring_launch(h, 0, RING_FLAT, G, G, p);
     return RAR_OK;
 }
 
@@ -344,46 +340,17 @@ int launch_tree_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     if ((long long)G * p > max_ctas) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
     cudaError_t ce = cudaMemsetAsync(h->recv_counts, 0, sizeof(unsigned long long) * (size_t)p, stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the send counters");
-    RingArgs a;
-    a.bufs = ptrs;
-    a.n = (long long)n;
-    a.first = 0;
-    a.n_total = (long long)n;
-    a.p = p;
+    RingArgs a = handle_ring_args(h, ptrs, p, n, 0, (long long)n);  // the tree's order ignores the index
     a.layout = TREE;
-    a.group = p;
     a.channels = G;
     a.fwd_channels = G;
-    a.split = (long long)n;
-    a.slice = 0;
-    a.first_step = 0;
-    a.n_steps = 0;
-    a.inv_p = 1.0f / (float)p;
-    a.epoch_word = h->epoch_words;
-    a.finish_count = h->epoch_words + 1;
-    a.flag_capacity = kMaxRingCtas;
-    a.flags = h->flags;
-    a.mailbox = h->ll_box;
-    a.mailbox_words = kLLMailboxWords;
     a.slot_words = slot_words;
-    a.recv_counts = h->recv_counts;
-    a.status = h->status;
-    a.abort_word = h->abort_word;
-    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
-    a.fault_mode = h->opt.fault_mode;
-    a.fault_rank = h->opt.fault_rank;
-    a.fault_delay_ns = h->opt.fault_delay_ns;
     ce = launch_tree_ll(a, dtype, op, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "tree grid cannot be co-resident");
         return cuda_fail(h, ce, "launching the low-latency tree");
     }
-    h->last_ring = true;
-    h->last_layout[0] = TREE;
-    h->last_channels[0] = G;
-    h->last_fwd_channels[0] = G;
-    h->last_group = p;
-    h->last_phases = 1;
+    note_ring_launch(h, 0, TREE, G, G, p);
     return RAR_OK;
 }
 
@@ -409,46 +376,17 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     while (((long long)n + slice - 1) / slice / G > kMaxSlicesPerChannelStep - 1) slice *= 2;
     cudaError_t ce = cudaMemsetAsync(h->recv_counts, 0, sizeof(unsigned long long) * (size_t)p, stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the send counters");
-    RingArgs a;
-    a.bufs = ptrs;
-    a.n = (long long)n;
-    a.first = 0;  // the tree's order does not depend on the index
-    a.n_total = (long long)n;
-    a.p = p;
+    RingArgs a = handle_ring_args(h, ptrs, p, n, 0, (long long)n);  // the tree's order ignores the index
     a.layout = TREE;
-    a.group = p;
     a.channels = G;
     a.fwd_channels = G;
-    a.split = (long long)n;
     a.slice = slice;
-    a.first_step = 0;
-    a.n_steps = 0;
-    a.inv_p = 1.0f / (float)p;
-    a.epoch_word = h->epoch_words;
-    a.finish_count = h->epoch_words + 1;
-    a.flag_capacity = kMaxRingCtas;
-    a.flags = h->flags;
-    a.mailbox = h->ll_box;
-    a.mailbox_words = kLLMailboxWords;
-    a.slot_words = 0;
-    a.recv_counts = h->recv_counts;
-    a.status = h->status;
-    a.abort_word = h->abort_word;
-    a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
-    a.fault_mode = h->opt.fault_mode;
-    a.fault_rank = h->opt.fault_rank;
-    a.fault_delay_ns = h->opt.fault_delay_ns;
     ce = launch_tree(a, dtype, op, vec16, threads, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "tree grid cannot be co-resident");
         return cuda_fail(h, ce, "launching the tree executor");
     }
-    h->last_ring = true;
-    h->last_layout[0] = TREE;
-    h->last_channels[0] = G;
-    h->last_fwd_channels[0] = G;
-    h->last_group = p;
-    h->last_phases = 1;
+    note_ring_launch(h, 0, TREE, G, G, p);
     return RAR_OK;
 }
 

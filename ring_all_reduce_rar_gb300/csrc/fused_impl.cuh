@@ -387,16 +387,8 @@ static int blocks_per_sm_of(K kernel, int threads) {
 }
 
 static int sm_count_cached() {
-    static int sms[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (sms[dev] == 0) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms[dev] = v > 0 ? v : 1;
-    }
-    return sms[dev];
+    const int v = current_device_sm_count();
+    return v > 0 ? v : 1;
 }
 
 template <typename K>

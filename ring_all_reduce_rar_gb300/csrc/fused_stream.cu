@@ -321,21 +321,24 @@ template <int DT, int OP, int VPT>
 static cudaError_t launch_stream_v(const FusedArgs &a, int tile_bytes, int n_stages, cudaStream_t stream) {
     auto kernel = fused_stream_kernel<DT, OP, VPT>;
     const size_t smem = (size_t)(n_stages + 2) * tile_bytes + 2 * kStreamMaxStages * sizeof(uint64_t);
-    static int configured_smem[64] = {0};
+    // the kernel's dynamic shared memory limit, raised once per device to
+    // the largest size asked for (setting it again is harmless)
+    static std::atomic<int> configured_smem[64];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if ((size_t)configured_smem[dev] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::atomic<int> &conf = configured_smem[dev >= 0 && dev < 64 ? dev : 0];
+    if ((size_t)conf.load(std::memory_order_relaxed) < smem || dev < 0 || dev >= 64) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured_smem[dev] = (int)smem;
+        conf.store((int)smem, std::memory_order_relaxed);
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStreamThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStreamThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_device_sm_count();
+    if (sms < 1) return cudaErrorInvalidDevice;
     const long long bulk_bytes = (a.n * ElemInfo<DT>::bytes) & ~15ll;
     const long long ntiles = (bulk_bytes + tile_bytes - 1) / tile_bytes;
     long long grid = (long long)sms * per_sm;

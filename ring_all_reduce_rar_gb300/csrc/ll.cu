@@ -346,9 +346,7 @@ int ll_max_coresident_ctas(bool tree, int dtype, int op) {
              : dispatch_dtype_op<true>(dtype, op, 0, [&](auto dt, auto o) {
                    return ll_occ_of(ring_ll_kernel<decltype(dt)::value, decltype(o)::value>);
                });
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_device_sm_count();
     return per_sm * sms;
 }
 

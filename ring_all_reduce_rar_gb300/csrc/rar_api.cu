@@ -577,8 +577,11 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
         delete h;
         return fail(nullptr, RAR_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(dg.err));
     }
-    cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
-    if (h->sm_count < 1) h->sm_count = 1;
+    h->sm_count = current_device_sm_count();
+    if (h->sm_count < 1) {
+        delete h;
+        return fail(nullptr, RAR_ECUDA, "querying the device's SM count failed");
+    }
     bool ok = cudaMalloc((void **)&h->flags, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
               cudaMalloc((void **)&h->recv_counts, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
               cudaMalloc((void **)&h->status, sizeof(RingStatus)) == cudaSuccess &&

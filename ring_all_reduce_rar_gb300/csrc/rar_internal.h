@@ -5,9 +5,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "rar.h"
 
 namespace rar {
+
+// SM count of the current device (cached per device ordinal; 0 if the
+// query fails, which callers treat as "nothing can be co-resident").
+inline int current_device_sm_count() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        int v = 0;
+        return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? v : 0;
+    }
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
 
 // Rank pointers travel in the kernel parameters for p <= kInlineP; larger p
 // read a device-side table kept in the handle's scratch.

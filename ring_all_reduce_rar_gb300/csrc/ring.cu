@@ -240,9 +240,7 @@ int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *ou
     const int per_sm = dispatch_dtype_op<true>(dtype, op, 0, [&](auto dt, auto o) {
         return ring_occ<decltype(dt)::value, decltype(o)::value>(vec16, threads);
     });
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_device_sm_count();
     if (out_per_sm) *out_per_sm = per_sm;
     return per_sm * sms;
 }

@@ -154,9 +154,7 @@ int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads) {
     const int per_sm = dispatch_dtype_op<false>(dtype, op, 0, [&](auto dt, auto o) {
         return tree_occ<decltype(dt)::value, decltype(o)::value>(vec16, threads);
     });
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_device_sm_count();
     return per_sm * sms;
 }
 

@@ -267,8 +267,9 @@ class Handle:
         self.h = rar_init(device, self.options)
 
     def set_options(self, **opts):
-        self.options = make_options(**opts)
-        rar_set_options(self.h, self.options)
+        options = make_options(**opts)
+        rar_set_options(self.h, options)  # raises, keeping the old options, if refused
+        self.options = options
 
     def allreduce(self, tensors, op="sum", stream=None):
         rar_allreduce(self.h, tensors, op, stream)

@@ -674,3 +674,25 @@ def test_argument_errors(rar, dev):
         with pytest.raises(rar.RarError) as e:
             h.allreduce([i[0], i[1]], op="avg")
         assert e.value.code == 2
+
+
+def test_option_errors(rar, dev):
+    """Out-of-range options are refused by rar_init and rar_set_options
+    (RAR_EINVAL), and the handle keeps its previous options."""
+    bad = [dict(engine=7), dict(protocol=3), dict(fused_path=5), dict(block_threads=100), dict(channels=-1),
+           dict(fault_mode=9), dict(hier_group=-2)]
+    for opts in bad:
+        with pytest.raises(rar.RarError) as e:
+            rar.Handle(0, **opts)
+        assert e.value.code == 1, opts
+    host = gen(4, 4099, "float32", ("uniform", -1.0, 1.0), 3)
+    ref, _ = oracle_expect(host, "float32", "sum", "ring")
+    with rar.Handle(0, engine="ring", protocol="ll") as h:
+        for opts in bad:
+            with pytest.raises(rar.RarError) as e:
+                h.set_options(**opts)
+            assert e.value.code == 1, opts
+        _, rows = upload(host, dev)
+        h.allreduce(rows)
+        h.check()
+        assert_bits_equal(rows, ref, "after refused options")

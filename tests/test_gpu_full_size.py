@@ -1,7 +1,8 @@
-"""GPU: the two large workloads -- p = 8, N = 2^30 bf16 (16 GiB, the
-benchmark's) and p = 64, N = 2^24 bf16 (2 GiB), N(0, 1e-2), sum -- checked
-against the oracle at every element, on the fused engine in the launch
-configuration the benchmark times (the streaming path).
+"""GPU: the large workloads checked against the oracle at every element, on
+the fused engine as the library picks its path: p = 8, N = 2^30 bf16
+(16 GiB, the benchmark's workload and launch configuration), p = 64,
+N = 2^24 bf16 and p = 8, N = 6,553,600 fp32, and the p = 16 sweep at
+N = 4^11 ... 4^13 (int32 sum, fp32 max, fp32 avg).
 
 The oracle's per-element fold ("Ring All-Reduce, in depth", "The
 schedule": element i of chunk c is x_c[i] (+) x_(c+1)[i] (+) ..., rounded
@@ -24,13 +25,19 @@ pytestmark = pytest.mark.gpu
 WINDOW = 1 << 24  # largest CPU window: elements per rank (32 MiB of bf16)
 
 
-@pytest.mark.parametrize("workload", ["p8_n1073741824_bf16", "p64_n16777216_bf16"])
-def test_full_size_every_element(rar, dev, workload):
-    cfg = w.WORKLOADS[workload]
-    p, n, dtype, dist, seed = cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"])
+CASES = [(name, cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"]), "sum")
+         for name, cfg in w.WORKLOADS.items() if cfg["n"] > 4 ** 10]
+# the p = 16 sweep above the sizes the other tests check element by element
+CASES += [(f"p16_n{n}_{w.SWEEP_PAIRS[k][0]}_{w.SWEEP_PAIRS[k][1]}", w.SWEEP_P, n, w.SWEEP_PAIRS[k][0],
+           w.SWEEP_PAIRS[k][2], w.seed_of(w.SWEEP_INDEX) + 16 * k, w.SWEEP_PAIRS[k][1])
+          for k in range(len(w.SWEEP_PAIRS)) for n in w.SWEEP_SIZES if n > 4 ** 10]
+
+
+@pytest.mark.parametrize("name,p,n,dtype,dist,seed,op", CASES, ids=[c[0] for c in CASES])
+def test_full_size_every_element(rar, dev, name, p, n, dtype, dist, seed, op):
     big, rows = w.make_inputs(p, n, dtype, dist, seed, device=dev)
     with rar.Handle(0, engine="fused") as h:
-        h.allreduce(rows)
+        h.allreduce(rows, op=op)
         h.check()
     for r in range(1, p):
         assert torch.equal(rows[r], rows[0]), f"rank {r} differs from rank 0"
@@ -44,7 +51,7 @@ def test_full_size_every_element(rar, dev, workload):
         idx = torch.arange(i0, min(n, i0 + window), dtype=torch.int64)
         vals = w.sample_inputs(seed, p, idx, dist, dtype)
         vals_np = np.stack([w.to_storage_numpy(vals[r]) for r in range(p)])
-        expect = oracle.fold_sampled(vals_np, idx.numpy(), n, dtype, "sum", "ring")
+        expect = oracle.fold_sampled(vals_np, idx.numpy(), n, dtype, op, "ring")
         bad = np.nonzero(got[i0:i0 + idx.numel()] != expect)[0]
         return i0, int(bad.size), (bad[:5] + i0).tolist()
 

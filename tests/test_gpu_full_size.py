@@ -2,7 +2,8 @@
 the fused engine as the library picks its path: p = 8, N = 2^30 bf16
 (16 GiB, the benchmark's workload and launch configuration), p = 64,
 N = 2^24 bf16 and p = 8, N = 6,553,600 fp32, and the p = 16 sweep at
-N = 4^11 ... 4^13 (int32 sum, fp32 max, fp32 avg).
+N = 4^11 ... 4^13 (int32 sum, fp32 max, fp32 avg); and the ring executor
+on the two largest.
 
 The oracle's per-element fold ("Ring All-Reduce, in depth", "The
 schedule": element i of chunk c is x_c[i] (+) x_(c+1)[i] (+) ..., rounded
@@ -25,18 +26,21 @@ pytestmark = pytest.mark.gpu
 WINDOW = 1 << 24  # largest CPU window: elements per rank (32 MiB of bf16)
 
 
-CASES = [(name, cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"]), "sum")
+CASES = [(name, "fused", cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"]), "sum")
          for name, cfg in w.WORKLOADS.items() if cfg["n"] > 4 ** 10]
+# the ring executor on the two largest workloads, as the benchmark times it
+CASES += [(name + "_ring", "ring", cfg["p"], cfg["n"], cfg["dtype"], cfg["dist"], w.seed_of(cfg["index"]), "sum")
+          for name, cfg in w.WORKLOADS.items() if cfg["n"] >= 1 << 24]
 # the p = 16 sweep above the sizes the other tests check element by element
-CASES += [(f"p16_n{n}_{w.SWEEP_PAIRS[k][0]}_{w.SWEEP_PAIRS[k][1]}", w.SWEEP_P, n, w.SWEEP_PAIRS[k][0],
+CASES += [(f"p16_n{n}_{w.SWEEP_PAIRS[k][0]}_{w.SWEEP_PAIRS[k][1]}", "fused", w.SWEEP_P, n, w.SWEEP_PAIRS[k][0],
            w.SWEEP_PAIRS[k][2], w.seed_of(w.SWEEP_INDEX) + 16 * k, w.SWEEP_PAIRS[k][1])
           for k in range(len(w.SWEEP_PAIRS)) for n in w.SWEEP_SIZES if n > 4 ** 10]
 
 
-@pytest.mark.parametrize("name,p,n,dtype,dist,seed,op", CASES, ids=[c[0] for c in CASES])
-def test_full_size_every_element(rar, dev, name, p, n, dtype, dist, seed, op):
+@pytest.mark.parametrize("name,engine,p,n,dtype,dist,seed,op", CASES, ids=[c[0] for c in CASES])
+def test_full_size_every_element(rar, dev, name, engine, p, n, dtype, dist, seed, op):
     big, rows = w.make_inputs(p, n, dtype, dist, seed, device=dev)
-    with rar.Handle(0, engine="fused") as h:
+    with rar.Handle(0, engine=engine) as h:
         h.allreduce(rows, op=op)
         h.check()
     for r in range(1, p):

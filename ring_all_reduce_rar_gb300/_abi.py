@@ -47,12 +47,13 @@ class Options(ctypes.Structure):
         ("fused_path", ctypes.c_int),
         ("hier_group", ctypes.c_int),
         ("protocol", ctypes.c_int),
+        ("slice_block", ctypes.c_int),
     ]
 
 
 def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, timeout_ns=0,
                  skip_pointer_check=False, fault_mode="none", fault_rank=0, fault_delay_ns=0,
-                 fused_path="auto", hier_group=0, protocol="auto") -> Options:
+                 fused_path="auto", hier_group=0, protocol="auto", slice_block=0) -> Options:
     o = Options()
     o.engine = ENGINE_CODES[engine] if isinstance(engine, str) else int(engine)
     o.channels = channels
@@ -66,6 +67,7 @@ def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, tim
     o.fused_path = FUSED_PATHS[fused_path] if isinstance(fused_path, str) else int(fused_path)
     o.hier_group = hier_group
     o.protocol = PROTOCOLS[protocol] if isinstance(protocol, str) else int(protocol)
+    o.slice_block = slice_block
     return o
 
 

@@ -157,6 +157,7 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.fwd_channels = G;
     a.split = (long long)n;
     a.slice = slice;
+    a.block = 0;
     a.first_step = 0;
     a.n_steps = 2 * (p - 1);
     a.inv_p = 1.0f / (float)p;

@@ -111,6 +111,7 @@ struct RingArgs {
                          // not bidirectional
     long long split;     // bidirectional: first global index of the second half (n_total otherwise)
     long long slice;     // elements per slice
+    long long block;     // slice positions per block of the processing order (0: all)
     int first_step;      // global schedule steps [first_step, first_step + n_steps)
     int n_steps;
     float inv_p;

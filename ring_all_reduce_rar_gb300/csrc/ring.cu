@@ -46,7 +46,8 @@ constexpr int kRingThreads = 512;
 constexpr int kRingUnroll = 4;
 
 // One slice [lo, hi) of one hop: dst = reduce ? op(src, dst) : src, then the
-// owner's avg scaling if `scale`.
+// owner's avg scaling if `scale`; 16-byte vectors where the slice is aligned
+// (VEC), single elements at its ends.
 template <int DT, int OP, bool VEC>
 __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
                                            bool scale, bool prescale_in, bool prescale_own, float inv_p) {
@@ -54,13 +55,15 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
     constexpr bool prediv = OP == OP_AVG_PREDIV;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
     const int T = blockDim.x;
-    long long vlo = (lo + VE - 1) / VE, vhi = hi / VE;
-    if (!VEC || vlo >= vhi) vlo = vhi = lo / VE;  // all of it on the element path
-    const long long elo = VEC ? vlo * VE : lo;      // [lo, elo) and [ehi, hi) per element
-    const long long ehi = VEC ? vhi * VE : lo;
-    // pre-divided average: a rank's original element enters scaled -- the
-    // receiver's own, and the incoming one at reduce-scatter step 0
-    auto one = [&](long long i) {
+    const long long vlo = (lo + VE - 1) / VE, vhi = hi / VE;
+    const bool vec_path = VEC && vlo < vhi;  // otherwise all of it on the element path
+    // single elements: [lo, vlo * VE) and [vhi * VE, hi), in one loop.
+    // Pre-divided average: a rank's original element enters scaled -- the
+    // receiver's own, and the incoming one at reduce-scatter step 0.
+    const long long n_head = vec_path ? vlo * VE - lo : hi - lo;
+    const long long n_tail = vec_path ? hi - vhi * VE : 0;
+    for (long long t = threadIdx.x; t < n_head + n_tail; t += T) {
+        const long long i = t < n_head ? lo + t : vhi * VE + (t - n_head);
         uint32_t x = load_elem<DT>(src, i);
         if (reduce) {
             if (prediv && prescale_in) x = scale_word<DT>(x, inv_p);
@@ -70,17 +73,8 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
         }
         if (OP == OP_AVG && scale) x = scale_word<DT>(x, inv_p);
         store_elem<DT>(dst, i, x);
-    };
-    if constexpr (!VEC) {
-        for (long long i = lo + threadIdx.x; i < hi; i += T) one(i);
-        return;
     }
-    if (vlo == vhi) {
-        for (long long i = lo + threadIdx.x; i < hi; i += T) one(i);
-        return;
-    }
-    for (long long i = lo + threadIdx.x; i < elo; i += T) one(i);
-    for (long long i = ehi + threadIdx.x; i < hi; i += T) one(i);
+    if (!vec_path) return;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
     for (long long v = vlo + threadIdx.x; v < vhi; v += (long long)T * kRingUnroll) {
@@ -112,6 +106,7 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
 template <int DT, int OP, bool VEC>
 __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __grid_constant__ RingArgs a) {
     __shared__ int s_stop;
+    __shared__ long long s_cs[RAR_MAX_P], s_ce[RAR_MAX_P], s_nsl[RAR_MAX_P];  // per chunk of the ring
     const int p = a.p;
     const int r = blockIdx.x / a.channels;
     const int j = blockIdx.x % a.channels;
@@ -157,47 +152,95 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
     const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
     const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
 
+    // the part of each chunk c of this rank's ring inside this launch's index
+    // range, in local indices (empty when the range misses the chunk), and
+    // its slice count: computed once per CTA
+    const long long gl = a.first, gh = a.first + a.n;
+    for (int c = threadIdx.x; c < rp; c += blockDim.x) {
+        long long cs = seg_lo + chunk_start(c, base, extra);
+        long long ce = seg_lo + chunk_start(c + 1, base, extra);
+        cs = (cs < gl ? gl : cs > gh ? gh : cs) - gl;
+        ce = (ce < gl ? gl : ce > gh ? gh : ce) - gl;
+        s_cs[c] = cs;
+        s_ce[c] = ce;
+        s_nsl[c] = (ce - cs + a.slice - 1) / a.slice;
+    }
+    // the chunk this rank receives at a schedule step
+    auto chunk_at = [&](int step) {
+        const bool rs = step < rp - 1;
+        const int s = rs ? step : step - (rp - 1);
+        if (fwd) return rs ? mod_p(pos - 1 - s, rp) : mod_p(pos - s, rp);
+        return rs ? mod_p(pos + 1 + s, rp) : mod_p(pos + s, rp);
+    };
+    // Processing order: blocks of K of this channel's slice positions
+    // (loc = 0, 1, ...); each block goes through every step before the next
+    // block starts.  K >= every step's slice count is the step-by-step order;
+    // a small K lets the right neighbour read a partial soon after it was
+    // written, while it is still in L2.  Progress words count the items
+    // (block, step, k) in this order, so they only grow; the item one step
+    // behind (block, step - 1, k) is K items earlier.
+    const long long nsl_max = (base + (extra > 0 ? 1 : 0) + a.slice - 1) / a.slice;  // the longest chunk's
+    // (at most 2^20 slice positions per channel and step: 32-bit counters)
+    const int max_locs = nsl_max > jj ? (int)((nsl_max - jj + GG - 1) / GG) : 0;
+    const int K = a.block > 0 && a.block < max_locs ? (int)a.block : (max_locs > 0 ? max_locs : 1);
+    const int S = a.n_steps;
+    __syncthreads();  // the chunk table
+
     if (!muted) {
-        for (int step = a.first_step; step < a.first_step + a.n_steps; step++) {
+        // items (block, step, k) in processing order: item = (blk * S + t) * K + k
+        const unsigned blocks = (unsigned)((max_locs + K - 1) / K);
+        const unsigned n_items = blocks * (unsigned)S * (unsigned)K;
+        int k = 0, t = 0, loc0 = 0;  // item's k and step, first slice position of its block
+        for (unsigned item = 0; item < n_items; item++) {
+            // (two equivalent decodes: whichever keeps the vector loop of this
+            // element size in registers, as measured with -Xptxas -v)
+            if constexpr (ElemInfo<DT>::bytes == 2) {
+                k = (int)(item % (unsigned)K);
+                const unsigned bt = item / (unsigned)K;
+                t = (int)(bt % (unsigned)S);
+                loc0 = (int)(bt / (unsigned)S) * K;
+            } else if (item > 0 && ++k == K) {  // next (block, step)
+                k = 0;
+                if (++t == S) {
+                    t = 0;
+                    loc0 += K;
+                }
+            }
+            const long long sl = jj + (long long)(loc0 + k) * GG;
+            const int step = a.first_step + t;
+            const int c = chunk_at(step);
+            if (sl >= s_nsl[c]) {  // (the same chunk, one step behind, has no such slice either)
+                item += (unsigned)(K - 1 - k);  // skip the rest of this (block, step)
+                k = K - 1;
+                continue;
+            }
             const bool rs = step < rp - 1;
             const int s = rs ? step : step - (rp - 1);
-            int c;
-            if (fwd) c = rs ? mod_p(pos - 1 - s, rp) : mod_p(pos - s, rp);
-            else c = rs ? mod_p(pos + 1 + s, rp) : mod_p(pos + s, rp);
-            // the part of chunk c inside this launch's index range, in
-            // local indices (empty when the range misses the chunk)
-            const long long gl = a.first, gh = a.first + a.n;
-            long long cs = seg_lo + chunk_start(c, base, extra);
-            long long ce = seg_lo + chunk_start(c + 1, base, extra);
-            cs = (cs < gl ? gl : cs > gh ? gh : cs) - gl;
-            ce = (ce < gl ? gl : ce > gh ? gh : ce) - gl;
-            const long long nsl = (ce - cs + a.slice - 1) / a.slice;
-            const bool scale = scale_here && rs && s == rp - 2;  // this rank becomes the chunk's owner
-            long long loc = 0;
-            for (long long sl = jj; sl < nsl; sl += GG, loc++) {
-                if (threadIdx.x == 0) {
-                    bool ok;
-                    if (step > a.first_step)
-                        ok = ring_wait(a, epoch, nb_flag, progress_tag(epoch, step - 1, loc), r, step, sl, nb);
-                    else
-                        ok = ld_relaxed_u32(a.abort_word) != epoch;
-                    if (ok && slow) ring_delay(a.fault_delay_ns);
-                    s_stop = ok ? 0 : 1;
-                }
-                __syncthreads();
-                if (s_stop) goto done;
-                {
-                    const long long lo = cs + sl * a.slice;
-                    const long long hi = lo + a.slice < ce ? lo + a.slice : ce;
-                    ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale, prediv_here && rs && s == 0, prediv_here,
-                                            a.inv_p);
-                    received += (unsigned long long)(hi - lo);
-                }
-                __syncthreads();
-                // the release store orders the CTA's slice stores (ordered
-                // before it by the barrier) ahead of the progress word
-                if (threadIdx.x == 0) st_release_u64(my_flag, progress_tag(epoch, step, loc));
+            if (threadIdx.x == 0) {
+                bool ok;
+                if (t > 0)
+                    ok = ring_wait(a, epoch, nb_flag, ((unsigned long long)epoch << 32) | (item - K + 1), r, step, sl,
+                                   nb);
+                else
+                    ok = ld_relaxed_u32(a.abort_word) != epoch;
+                if (ok && slow) ring_delay(a.fault_delay_ns);
+                s_stop = ok ? 0 : 1;
             }
+            __syncthreads();
+            if (s_stop) goto done;
+            {
+                const long long ce = s_ce[c];
+                const long long lo = s_cs[c] + sl * a.slice;
+                const long long hi = lo + a.slice < ce ? lo + a.slice : ce;
+                // scale: this rank becomes the chunk's owner
+                ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale_here && rs && s == rp - 2,
+                                        prediv_here && rs && s == 0, prediv_here, a.inv_p);
+                received += (unsigned long long)(hi - lo);
+            }
+            __syncthreads();
+            // the release store orders the CTA's slice stores (ordered
+            // before it by the barrier) ahead of the progress word
+            if (threadIdx.x == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
         }
     }
 done:

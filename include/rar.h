@@ -157,12 +157,13 @@ typedef struct {
                                       ring, while p * 2 (p - 1) chunk-sized slots fit in
                                       RAR_LL_MAILBOX_BYTES; tree: while
                                       p * (ceil(log2 p) + 1) buffer-sized slots fit */
-    int slice_block;               /* RAR_ENGINE_RING / RING_BIDIR with progress words: each
+    int slice_block;               /* ring and tree executors with progress words: each
                                       channel takes its slices in blocks of this many and runs
                                       a block through every step before the next, so that the
-                                      neighbour reads a partial while it is still in L2
-                                      (0 = auto; a value at least the slices per step gives the
-                                      step-by-step order).  Results do not depend on it. */
+                                      reader finds a fresh slice still in L2 (0 = auto: 1 for
+                                      the ring, 2 for the tree; a value at least the slices per
+                                      step gives the step-by-step order).  Results do not
+                                      depend on it. */
 } rar_options;
 
 /* Bytes of the low-latency mailbox each handle allocates in rar_init. */

@@ -3,8 +3,9 @@
 // bounded waits, and the status word a wait that runs out fills in.
 //
 // A CTA publishes its progress after each slice with a release store of a
-// 64-bit word (epoch << 32) | (step << 20) | (slice-within-channel + 1); a
-// waiter acquires it.  Epoch-tagged words need no reset between calls.
+// 64-bit word (epoch << 32) | (items done), counting the items (slice block,
+// step, slice) of its processing order; a waiter acquires it.  Epoch-tagged
+// words need no reset between calls.
 // Every wait is bounded by the call's timeout (globaltimer) and an
 // iteration cap; the first CTA to give up records where, raises the abort
 // word (which every other wait polls) and returns.  Nothing traps.
@@ -31,10 +32,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-
-__device__ __forceinline__ unsigned long long progress_tag(unsigned epoch, int step, long long loc) {
-    return ((unsigned long long)epoch << 32) | ((unsigned long long)step << 20) | (unsigned long long)(loc + 1);
 }
 
 __device__ __forceinline__ int mod_p(int v, int p) {

@@ -380,7 +380,8 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     long long slice = h->opt.slice_elems;
     if (slice == 0) {
         slice = ((long long)n + G - 1) / G;
-        slice = std::min<long long>(std::max<long long>((slice + 1023) / 1024 * 1024, 1024), 65536);
+        slice = std::min<long long>(std::max<long long>((slice + 1023) / 1024 * 1024, 1024),
+                                    kRingMaxSliceBytes / elem_bytes(dtype));
     }
     slice = std::max<long long>(16, (slice + 15) / 16 * 16);
     while (((long long)n + slice - 1) / slice / G > kMaxSlicesPerChannelStep - 1) slice *= 2;
@@ -391,6 +392,10 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     a.channels = G;
     a.fwd_channels = G;
     a.slice = slice;
+    // slice order: two slice positions at a time through every level (p = 8,
+    // 16 GiB bf16 on GB300: 11.9 ms, against 12.2 one at a time and 13.7
+    // level by level; a reader finds the child's or parent's fresh slice in L2)
+    a.block = h->opt.slice_block ? h->opt.slice_block : 2;
     ce = launch_tree(a, dtype, op, vec16, threads, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "tree grid cannot be co-resident");

@@ -17,15 +17,15 @@
 // Element moves: (p - 1) reduce hops of 3 moves and (p - 1) broadcast hops of
 // 2, the same 5 (p - 1) n as the ring.
 //
-// Hand-offs use the progress words of flag_sync.cuh; a rank with nothing to
-// do at a step publishes the step as passed so that waiters move on.  Every
-// wait is bounded.
+// Hand-offs use the progress words of flag_sync.cuh, counting items (slice
+// block, step, slice) in processing order; a rank with nothing to do at a
+// step still passes its items so that waiters move on.  Every wait is
+// bounded.
 #include "flag_sync.cuh"
 
 namespace rar {
 
 constexpr int kTreeThreads = 512;
-constexpr long long kTreePassLoc = (1ll << 20) - 2;  // "whole step passed"
 
 // One slice [lo, hi): reduce: dst = op(dst, src) (+ the root's avg scaling);
 // broadcast: dst = src.
@@ -59,7 +59,7 @@ __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long
 }
 
 template <int DT, int OP, bool VEC>
-__global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __grid_constant__ RingArgs a) {
+__global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __grid_constant__ RingArgs a) {
     __shared__ int s_stop;
     const int p = a.p;
     const int r = blockIdx.x / a.channels;
@@ -71,48 +71,73 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_executor_kernel(const __
     const long long nsl = (a.n + a.slice - 1) / a.slice;
     const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
     const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
+    // Processing order, as in the ring executor: this channel's slice
+    // positions (loc = 0, 1, ...) in blocks of K, each block through every
+    // step before the next, so that a reader finds the slice it waited for
+    // still in L2; progress words count the items (block, step, k) in this
+    // order, and a rank with nothing to do at a step still passes its items.
+    const int max_locs = nsl > j ? (int)((nsl - j + a.channels - 1) / a.channels) : 0;
+    const int K = a.block > 0 && a.block < max_locs ? (int)a.block : (max_locs > 0 ? max_locs : 1);
+    const int S = 2 * L;
+    const unsigned n_items = (unsigned)((max_locs + K - 1) / K) * (unsigned)S * (unsigned)K;
     const unsigned epoch = launch_epoch_begin(a);
     if (muted) goto done;
 
-    for (int t = 0; t < 2 * L; t++) {
-        const bool up = t < L;
-        const int l = up ? t : 2 * L - 1 - t;
-        const int span = 1 << l;
-        int peer = -1;  // the rank read at this step
-        if (up) {
-            if ((r & (2 * span - 1)) == 0 && r + span < p) peer = r + span;
-        } else {
-            if ((r & (2 * span - 1)) == span) peer = r - span;
-        }
-        if (peer < 0) {
-            // nothing to do: the step is passed as soon as the previous one is
-            if (threadIdx.x == 0) st_release_u64(my_flag, progress_tag(epoch, t, kTreePassLoc));
-            continue;
-        }
-        const char *src = rank_ptr(a.bufs, p, peer);
-        const unsigned long long *peer_flag = a.flags + (long long)peer * a.channels + j;
-        const bool root_last = up && r == 0 && l == L - 1;
-        long long loc = 0;
-        for (long long sl = j; sl < nsl; sl += a.channels, loc++) {
-            if (threadIdx.x == 0) {
-                // the peer's data is final for this slice once it passed step t - 1
-                bool ok = t > 0 ? ring_wait(a, epoch, peer_flag, progress_tag(epoch, t - 1, loc), r, t, sl, peer)
-                                : ld_relaxed_u32(a.abort_word) != epoch;
-                if (ok && slow) ring_delay(a.fault_delay_ns);
-                s_stop = ok ? 0 : 1;
+    {
+        int k = 0, t = 0, loc0 = 0;  // item's k and step, first slice position of its block
+        for (unsigned item = 0; item < n_items; item++) {
+            if (item > 0 && ++k == K) {  // next (block, step)
+                k = 0;
+                if (++t == S) {
+                    t = 0;
+                    loc0 += K;
+                }
             }
-            __syncthreads();
-            if (s_stop) goto done;
-            const long long lo = sl * a.slice;
-            const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
-            tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, root_last, a.inv_p);
-            __syncthreads();
-            // the release store orders the CTA's slice stores (ordered
-            // before it by the barrier) ahead of the progress word
-            if (threadIdx.x == 0) {
-                atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // elements the peer sent
-                st_release_u64(my_flag, progress_tag(epoch, t, loc));
+            const long long sl = j + (long long)(loc0 + k) * a.channels;
+            if (sl >= nsl) {  // past the last slice: the rest of this (block, step) is empty too
+                item += (unsigned)(K - 1 - k);
+                k = K - 1;
+                continue;
             }
+            const bool up = t < L;
+            const int l = up ? t : 2 * L - 1 - t;
+            const int span = 1 << l;
+            int peer = -1;  // the rank read at this step
+            if (up) {
+                if ((r & (2 * span - 1)) == 0 && r + span < p) peer = r + span;
+            } else {
+                if ((r & (2 * span - 1)) == span) peer = r - span;
+            }
+            if (peer < 0) {
+                // nothing to do at this step: pass the whole (block, step) at once
+                item += (unsigned)(K - 1 - k);
+                k = K - 1;
+                if (threadIdx.x == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
+                continue;
+            }
+            {
+                const char *src = rank_ptr(a.bufs, p, peer);
+                const unsigned long long *peer_flag = a.flags + (long long)peer * a.channels + j;
+                if (threadIdx.x == 0) {
+                    // the peer's data is final for this slice once it passed
+                    // the same slice at step t - 1 (K items earlier)
+                    bool ok = t > 0 ? ring_wait(a, epoch, peer_flag, ((unsigned long long)epoch << 32) | (item - K + 1),
+                                                r, t, sl, peer)
+                                    : ld_relaxed_u32(a.abort_word) != epoch;
+                    if (ok && slow) ring_delay(a.fault_delay_ns);
+                    s_stop = ok ? 0 : 1;
+                }
+                __syncthreads();
+                if (s_stop) goto done;
+                const long long lo = sl * a.slice;
+                const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
+                tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, up && r == 0 && l == L - 1, a.inv_p);
+                __syncthreads();
+                if (threadIdx.x == 0) atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // the peer sent
+            }
+            // the release store orders the CTA's slice stores (ordered before
+            // it by the barrier) ahead of the progress word
+            if (threadIdx.x == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
         }
     }
 done:

@@ -42,7 +42,7 @@ using namespace rar;
 constexpr int kNoAllocMaxCtas = 1024;
 constexpr int kNoAllocMaxDevices = 64;
 constexpr int kNoAllocThreads = 256;
-constexpr long long kNoAllocSlice = 65536;
+constexpr long long kNoAllocSliceBytes = 128 << 10;
 constexpr unsigned long long kNoAllocTimeoutNs = 2000000000ull;
 
 // Layout of the scratch array.
@@ -138,9 +138,9 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
         scratch = slot.scratch;
     }
 
-    // slices: at most 64K elements, and few enough per channel and step to fit
-    // the progress word's 20-bit field
-    long long slice = kNoAllocSlice;
+    // slices: at most 128 KB, and at most 2^20 - 2 slice positions per
+    // channel and step (the progress words count 32-bit items)
+    long long slice = kNoAllocSliceBytes / (long long)e;
     const long long maxchunk = ((long long)n + p - 1) / p;
     while ((maxchunk + slice - 1) / slice / G > (1ll << 20) - 2) slice *= 2;
 
@@ -157,7 +157,7 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.fwd_channels = G;
     a.split = (long long)n;
     a.slice = slice;
-    a.block = 0;
+    a.block = 1;  // one slice position at a time through every step, as the handle's default
     a.first_step = 0;
     a.n_steps = 2 * (p - 1);
     a.inv_p = 1.0f / (float)p;

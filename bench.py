@@ -10,6 +10,7 @@ ranks, N = 2^30 bf16 elements per rank (16 GiB in total, far above the
     python bench.py --sweep [--pair 0|1|2] # p = 16, N = 4^5 ... 4^13, every engine
     python bench.py --configs             # every workload on every engine
     python bench.py --hops                # smallest buffers, p = 2 ... 64
+    python bench.py --next                # the widened rows on the 16 GiB shape
 
 Metric: algBW = p * N * element bytes / time per step (GB/s), summed over
 GPUs when run under torchrun (independent replicas, weak scaling).  Also
@@ -397,6 +398,77 @@ def run_hops(args):
         print(json.dumps(line), flush=True)
 
 
+def run_next(args):
+    """The widened rows on the 16 GiB workload shape (p = 8, N = 2^30), device
+    time per call and the fraction of each one's minimum-traffic roofline, one
+    JSON line each: reduce-scatter and all-gather alone, the hierarchical
+    schedule, and fp16 with the post- and pre-divided average."""
+    import ring_all_reduce_rar_gb300 as rar
+    rar.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak = hbm_peak()[0]
+    cfg = w.WORKLOADS["p8_n1073741824_bf16"]
+    p, n, e = cfg["p"], cfg["n"], 2
+
+    def emit(row, engine, us, bytes_):
+        print(json.dumps({"row": row, "engine": engine, "p": p, "n": n, "us_per_call": round(us, 2),
+                          "algbw_gbs": round(p * n * e / us / 1e3, 2), "roofline_bytes": bytes_,
+                          "roofline_frac": round(bytes_ / us / 1e3 / peak, 4)}), flush=True)
+
+    big, rows = w.make_inputs(p, n, "bfloat16", cfg["dist"], w.seed_of(cfg["index"]), device=dev)
+    # reduce-scatter and all-gather alone ("Ring All-Reduce, in depth",
+    # "Trade-offs").  Minimum bytes: the fused reduce-scatter reads every rank
+    # and writes the owner's chunk, (p + 1) N e; its all-gather reads the owner
+    # and writes the p - 1 others, p N e; the ring's halves move 3 (p - 1) N e
+    # and 2 (p - 1) N e.
+    for eng, rs_bytes, ag_bytes in [("fused", (p + 1) * n * e, p * n * e),
+                                    ("ring", 3 * (p - 1) * n * e, 2 * (p - 1) * n * e)]:
+        for fn, b in [("reduce_scatter", rs_bytes), ("all_gather", ag_bytes)]:
+            emit(fn, eng, device_us_per_call_fn(rar, VARIANTS[eng], rows, fn, 10), b)
+    # hierarchical 2D schedule ("Ring All-Reduce, in depth", "Hierarchy"):
+    # the same minimum bytes as the flat engines
+    for g in (2, 4):
+        for eng in ("fused", "ring"):
+            opts = dict(VARIANTS[eng], hier_group=g)
+            if eng == "fused":
+                opts["fused_path"] = "registers"  # the hierarchical order runs on the per-thread path
+            emit(f"hierarchical g={g}", eng, device_us_per_call(rar, opts, rows, "sum", 10),
+                 2 * p * n * e if eng == "fused" else 5 * (p - 1) * n * e)
+    del big, rows
+    torch.cuda.empty_cache()
+    # fp16 with the post- and pre-divided average ("Ring All-Reduce, in
+    # depth", "Failure modes")
+    big, rows = w.make_inputs(p, n, "float16", cfg["dist"], w.seed_of(cfg["index"]), device=dev)
+    for op in ("sum", "avg", "avg_prediv"):
+        for eng in ("fused", "ring"):
+            emit(f"fp16 {op}", eng, device_us_per_call(rar, VARIANTS[eng], rows, op, 10),
+                 2 * p * n * e if eng == "fused" else 5 * (p - 1) * n * e)
+    del big, rows
+    torch.cuda.empty_cache()
+
+
+def device_us_per_call_fn(rar, opts, rows, fn, k):
+    """As device_us_per_call, for the handle method `fn` (reduce_scatter,
+    all_gather) on the rank buffers."""
+    with rar.Handle(0, skip_pointer_check=True, **opts) as h:
+        call = getattr(h, fn)
+        for _ in range(3):
+            call(rows)
+        h.check()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000_000)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(k):
+            call(rows)
+        end.record()
+        torch.cuda.synchronize()
+        if h.status() != 0:
+            raise RuntimeError(rar.rar_last_error(h.h))
+        return start.elapsed_time(end) * 1e3 / k
+
+
 def device_us_per_call(rar, opts, rows, op, k):
     """Device time per call: the GPU is held by a short sleep kernel while
     the host queues k calls, so events time back-to-back execution only."""
@@ -496,6 +568,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="device time per call over the p = 16 message-size sweep (not the benchmark line)")
     ap.add_argument("--pair", type=int, default=0, help="--sweep: dtype/op pair of the sweep workload (0..2)")
+    ap.add_argument("--next", action="store_true",
+                    help="reduce-scatter / all-gather alone, the hierarchical schedule, fp16 averages (16 GiB shape)")
     ap.add_argument("--hops", action="store_true",
                     help="per-call time of the smallest buffers for p = 2 ... 64 (fixed cost + step latency)")
     ap.add_argument("--configs", action="store_true",
@@ -512,6 +586,8 @@ def main():
         run_sweep(args)
     elif args.hops:
         run_hops(args)
+    elif args.next:
+        run_next(args)
     elif args.configs:
         run_configs(args)
     elif args.impl == "reference":

@@ -377,6 +377,82 @@ __global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel(const __grid_
     }
 }
 
+// The same order with all P ranks' vectors in flight at once (P a
+// compile-time rank count): each thread keeps the rank order of the fold for
+// its current (intra-node chunk, sub-chunk) segment and rebuilds it only when
+// its vectors move into another segment, so a vector costs P loads, the fold
+// and P stores.  Vectors across a segment boundary fold element by element.
+template <int DT, int OP, int P, bool VEC>
+__global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel_p(const __grid_constant__ FusedArgs a, int g) {
+    constexpr int hop = HopOf<OP>::value;
+    constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
+    const int m = P / g;
+    const long long n = a.n;
+    const long long nt = a.n_total, g0 = a.first;
+    const long long nvec = (n + VE - 1) / VE;
+    const long long nfull = n / VE;
+    long long seg_lo = 1, seg_hi = 0;  // current segment, global indices [seg_lo, seg_hi); none yet
+    int ord[P];                        // its ranks in fold order
+    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (long long)gridDim.x * blockDim.x) {
+        const long long e0 = v * VE;
+        const long long ge0 = g0 + e0;
+        if (ge0 < seg_lo || ge0 >= seg_hi) {
+            const HierPos hp = hier_pos(ge0, nt, g, m);
+            const long long gb = nt / g, ge = nt % g;
+            const long long c0 = chunk_start(hp.c, gb, ge);
+            const long long len = gb + (hp.c < ge ? 1 : 0);
+            seg_lo = c0 + chunk_start(hp.s, len / m, len % m);
+            seg_hi = c0 + chunk_start(hp.s + 1, len / m, len % m);
+            int t = 0, kk = 0;
+#pragma unroll
+            for (int k = 0; k < P; k++) {
+                int node = hp.s + t;
+                node -= node >= m ? m : 0;
+                int l = hp.c + kk;
+                l -= l >= g ? g : 0;
+                ord[k] = node * g + l;
+                if (++kk == g) {
+                    kk = 0;
+                    t++;
+                }
+            }
+        }
+        if (VEC && v < nfull && ge0 + VE <= seg_hi) {
+            uint4 x[P];
+#pragma unroll
+            for (int k = 0; k < P; k++)
+                x[k] = contrib_vec<DT, OP>(__ldcs(reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, P, ord[k])) + v),
+                                           a.inv_p);
+            // node partials over g local ranks, then over the nodes in turn
+            uint4 acc = x[0], part = x[0];
+            int kk = 1;
+#pragma unroll
+            for (int k = 1; k < P; k++) {
+                if (kk == g) {
+                    acc = k == g ? part : hop_vec<DT, hop>(acc, part);
+                    part = x[k];
+                    kk = 1;
+                } else {
+                    part = hop_vec<DT, hop>(part, x[k]);
+                    kk++;
+                }
+            }
+            acc = g == P ? part : hop_vec<DT, hop>(acc, part);
+            if constexpr (OP == OP_AVG) acc = scale_vec<DT>(acc, a.inv_p);
+#pragma unroll
+            for (int r = 0; r < P; r++) __stcs(reinterpret_cast<uint4 *>(rank_ptr(a.bufs, P, r)) + v, acc);
+            continue;
+        }
+        for (int l = 0; l < VE; l++) {
+            const long long i = e0 + l;
+            if (i >= n) break;
+            const uint32_t acc = hier_fold_element<DT, OP>(a, P, g, hier_pos(g0 + i, nt, g, m), i);
+            for (int r = 0; r < P; r++) store_elem<DT>(rank_ptr(a.bufs, P, r), i, acc);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- dispatch
 
 template <typename K>

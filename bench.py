@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -69,14 +70,23 @@ ENGINE_SOURCES = {
 ENGINE_SOURCES["ring_bidir"] = ENGINE_SOURCES["ring"]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and blank lines (string literals in
+    these sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(engine: str) -> str:
-    """Hash of the CUDA sources behind one engine's kernel, to tell whether
-    stored ncu counters still describe the kernel being timed."""
+    """Hash of the code (comments dropped) of the CUDA sources behind one
+    engine's kernel, to tell whether stored ncu counters still describe the
+    kernel being timed."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ring_all_reduce_rar_gb300", "csrc")
     for name in ENGINE_SOURCES[engine]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,18 +12,22 @@
 // Pipelining ("What real libraries add", "Pipelining"): each chunk is cut
 // into slices of `slice` elements; slice k belongs to channel k mod
 // channels, and every channel is an independent ring over its slices
-// ("Multiple rings, or channels").  A CTA publishes its progress after each
-// slice with a release store of a 64-bit word
-//     (epoch << 32) | (step << 20) | (slice-within-channel + 1),
+// ("Multiple rings, or channels").  A channel takes its slice positions in
+// blocks of `block` and runs each block through every step before the next
+// (one position at a time by default), so the right neighbour rereads a
+// fresh partial while it is still in L2.  A CTA publishes its progress
+// after each slice with a release store of a 64-bit word
+//     (epoch << 32) | (items done in this order),
 // and the right neighbour's CTA of the same channel acquires it before it
 // reads that slice at the next step.  The epoch comes from device memory
 // (flag_sync.cuh), so the words need no reset between launches and a launch
 // captured in a CUDA graph can be replayed.
 //
-// In-place safety: rank r - 1 overwrites the chunk r read at reduce-scatter
-// step s only at its all-gather step s, and that write waits on a chain of
-// flags that starts with r's own release after the read (the chunk's
-// remaining reduce-scatter hops, its owner, the all-gather hops up to r - 1).
+// In-place safety, per slice of a chunk and so in any processing order:
+// rank r - 1 overwrites the slice r read at reduce-scatter step s only at its
+// all-gather step s, and that write waits on a chain of flags that starts
+// with r's own release after the read (the chunk's remaining reduce-scatter
+// hops, its owner, the all-gather hops up to r - 1).
 //
 // Bidirectional variant ("Bidirectional rings"): channels
 // [fwd_channels, channels) run the mirrored ring (send to r - 1) on the

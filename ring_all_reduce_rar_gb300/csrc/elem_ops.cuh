@@ -109,19 +109,20 @@ __device__ __forceinline__ uint32_t hop_word(uint32_t acc, uint32_t own) {
     }
 }
 
-// avg epilogue: x * (1/p) in binary32, rounded once, then to the 16-bit type.
+// avg epilogue: x * (1/p) in binary32, rounded once, then to the 16-bit type
+// (both lanes of a word converted by one paired round-to-nearest).
 template <int DT>
 __device__ __forceinline__ uint32_t scale_word(uint32_t w, float inv_p) {
     if constexpr (DT == DT_F32) {
         return __float_as_uint(__fmul_rn(__uint_as_float(w), inv_p));
     } else if constexpr (DT == DT_BF16) {
-        uint32_t lo = float_to_bf16_bits(__fmul_rn(bf16_bits_to_float(w & 0xFFFFu), inv_p));
-        uint32_t hi = float_to_bf16_bits(__fmul_rn(bf16_bits_to_float(w >> 16), inv_p));
-        return lo | (hi << 16);
+        const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+        __nv_bfloat162 r = __floats2bfloat162_rn(__fmul_rn(lo, inv_p), __fmul_rn(hi, inv_p));
+        return *reinterpret_cast<uint32_t *>(&r);
     } else if constexpr (DT == DT_F16) {
-        uint32_t lo = float_to_f16_bits(__fmul_rn(f16_bits_to_float(w & 0xFFFFu), inv_p));
-        uint32_t hi = float_to_f16_bits(__fmul_rn(f16_bits_to_float(w >> 16), inv_p));
-        return lo | (hi << 16);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+        __half2 r = __floats2half2_rn(__fmul_rn(f.x, inv_p), __fmul_rn(f.y, inv_p));
+        return *reinterpret_cast<uint32_t *>(&r);
     } else {
         return w;
     }

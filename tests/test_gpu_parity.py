@@ -375,6 +375,33 @@ def test_ring_race_check_slices_and_channels(rar, dev):
             assert_bits_equal(rows, r2 if engine == "ring_bidir" else ref, f"{engine} ch={ch} sl={sl}")
 
 
+@pytest.mark.parametrize("engine,extra", [("ring", {}), ("ring_bidir", {}), ("ring", dict(hier_group=2)),
+                                          ("tree", {})])
+def test_slice_order_does_not_change_results(rar, dev, engine, extra):
+    """slice_block (slice positions per block of the processing order) only
+    reorders the hand-offs: any block size, with several slices per channel
+    and step, gives the same bits and send counts."""
+    p, n = 8, 8 * 30000 + 13
+    host = gen(p, n, "bfloat16", ("normal", 1e-2), 23)
+    if extra.get("hier_group"):
+        ref = [w.to_storage_numpy(t).copy() for t in host]
+        intra, inter = oracle.hier_simulate(ref, extra["hier_group"], "bfloat16", "sum")
+        sends = list(intra + inter)
+    else:
+        ref, sends = oracle_expect(host, "bfloat16", "sum", engine)
+    for blk in [1, 2, 3, 7, 1 << 20]:
+        _, rows = upload(host, dev)
+        with rar.Handle(0, **handle_opts(engine, channels=3, slice_elems=1024, slice_block=blk, **extra)) as h:
+            h.allreduce(rows)
+            h.check()
+            got = h.send_counts(p)
+        assert_bits_equal(rows, ref, f"{engine} {extra} slice_block={blk}")
+        if engine == "tree":
+            assert sum(got) == 2 * (p - 1) * n
+        else:
+            assert got == list(sends)
+
+
 def test_ring_back_to_back_calls_reuse_flags(rar, dev):
     host = gen(4, 4099, "float32", ("uniform", -1.0, 1.0), 3)
     ref, _ = oracle_expect(host, "float32", "sum", "ring")

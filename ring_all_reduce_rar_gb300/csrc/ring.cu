@@ -7,7 +7,11 @@
 // all-gather step s it receives chunk (r - s) mod p and overwrites its copy.
 // Data moves through the rank buffers themselves (the receiver reads the
 // sender's copy in place), so a reduce-scatter hop costs 3 element moves
-// (read incoming, read own, write own) and an all-gather hop 2.
+// (read incoming, read own, write own) and an all-gather hop 2.  A partial
+// that has been handed on is dead until its owner's all-gather step
+// overwrites it, so in a launch of the whole schedule the receiver drops
+// its lines from L2 once it has read them: a partial still in L2 then never
+// reaches DRAM.
 //
 // Pipelining ("What real libraries add", "Pipelining"): each chunk is cut
 // into slices of `slice` elements; slice k belongs to channel k mod
@@ -54,7 +58,8 @@ constexpr int kRingUnroll = 4;
 // (VEC), single elements at its ends.
 template <int DT, int OP, bool VEC>
 __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
-                                           bool scale, bool prescale_in, bool prescale_own, float inv_p) {
+                                           bool scale, bool prescale_in, bool prescale_own, bool discard_src,
+                                           float inv_p) {
     constexpr int hop_op = HopOf<OP>::value;
     constexpr bool prediv = OP == OP_AVG_PREDIV;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
@@ -105,6 +110,26 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
             }
         }
     }
+    if (!discard_src) return;
+    // The incoming partial is dead once read: its owner overwrites it at its
+    // all-gather step, and nobody reads it before that.  Drop its dirty
+    // lines from L2 without writing them back (PTX discard.global.L2: the
+    // line then holds an indeterminate value until it is written again).
+    // Warp w read the 32 vectors [vlo + 32 w + m T, + 32) for every m; after
+    // __syncwarp, which orders the warp's reads before it, lane l drops line
+    // l % 4 of segment m = l / 4 (mod 8) if the 128-byte line lies wholly in
+    // that segment.  The barrier and release store that publish the slice
+    // come after, so the owner's all-gather write, which waits on a chain of
+    // progress words that starts there, is ordered after the discard.
+    __syncwarp();
+    const int lane = threadIdx.x & 31;
+    const uintptr_t end = reinterpret_cast<uintptr_t>(s4 + vhi);
+    for (long long s0 = vlo + 32ll * (threadIdx.x >> 5) + (long long)(lane >> 2) * T; s0 < vhi; s0 += 8ll * T) {
+        const uintptr_t seg = reinterpret_cast<uintptr_t>(s4 + s0);
+        const uintptr_t line = ((seg + 127) & ~(uintptr_t)127) + 128u * (unsigned)(lane & 3);
+        const uintptr_t seg_end = seg + 512 < end ? seg + 512 : end;
+        if (line + 128 <= seg_end) asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+    }
 }
 
 template <int DT, int OP, bool VEC>
@@ -147,6 +172,10 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
     // contribution once, where it enters the reduction
     const bool scale_here = OP == OP_AVG && a.layout != RING_INTRA;
     const bool prediv_here = OP == OP_AVG_PREDIV && a.layout != RING_INTER;
+    // a launch of the whole flat schedule overwrites every partial it hands
+    // over with the chunk's final value before it ends: the receiver drops
+    // the partial's lines from L2 once read (ring_slice)
+    const bool discard_partials = a.layout == RING_FLAT && a.first_step == 0 && a.n_steps == 2 * (rp - 1);
     const char *src = rank_ptr(a.bufs, p, nb);
     char *dst = rank_ptr(a.bufs, p, r);
     unsigned long long *my_flag = a.flags + blockIdx.x;
@@ -238,7 +267,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
                 const long long hi = lo + a.slice < ce ? lo + a.slice : ce;
                 // scale: this rank becomes the chunk's owner
                 ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale_here && rs && s == rp - 2,
-                                        prediv_here && rs && s == 0, prediv_here, a.inv_p);
+                                        prediv_here && rs && s == 0, prediv_here, discard_partials && rs && s > 0,
+                                        a.inv_p);
                 received += (unsigned long long)(hi - lo);
             }
             __syncthreads();

@@ -115,6 +115,28 @@ __device__ __forceinline__ void launch_epoch_end(const RingArgs &a, unsigned epo
     }
 }
 
+// Drop dead data from L2 without writing it back (PTX discard.global.L2:
+// the line then holds an indeterminate value until it is written again).
+// For a slice that the CTA's vector loop has just read, thread t taking the
+// vectors vlo + t + m T of [vlo, vhi): warp w read the 32 vectors
+// [vlo + 32 w + m T, + 32) for every m, so after __syncwarp, which orders
+// the warp's reads before it, the warp may drop any 128-byte line that lies
+// wholly in one of its segments -- lane l takes line l % 4 of segment
+// m = l / 4 (mod 8).  The caller publishes the slice after this (barrier and
+// release store), so a write that waits on that publication is ordered
+// after the discard.
+__device__ __forceinline__ void discard_read_lines(const uint4 *s4, long long vlo, long long vhi, int T) {
+    __syncwarp();
+    const int lane = threadIdx.x & 31;
+    const uintptr_t end = reinterpret_cast<uintptr_t>(s4 + vhi);
+    for (long long s0 = vlo + 32ll * (threadIdx.x >> 5) + (long long)(lane >> 2) * T; s0 < vhi; s0 += 8ll * T) {
+        const uintptr_t seg = reinterpret_cast<uintptr_t>(s4 + s0);
+        const uintptr_t line = ((seg + 127) & ~(uintptr_t)127) + 128u * (unsigned)(lane & 3);
+        const uintptr_t seg_end = seg + 512 < end ? seg + 512 : end;
+        if (line + 128 <= seg_end) asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+    }
+}
+
 // Injected straggler: pause about `ns` (bounded by the same clock).
 static __device__ void ring_delay(unsigned ns) {
     const unsigned long long t0 = global_ns();

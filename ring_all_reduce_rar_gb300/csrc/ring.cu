@@ -110,26 +110,10 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
             }
         }
     }
-    if (!discard_src) return;
     // The incoming partial is dead once read: its owner overwrites it at its
-    // all-gather step, and nobody reads it before that.  Drop its dirty
-    // lines from L2 without writing them back (PTX discard.global.L2: the
-    // line then holds an indeterminate value until it is written again).
-    // Warp w read the 32 vectors [vlo + 32 w + m T, + 32) for every m; after
-    // __syncwarp, which orders the warp's reads before it, lane l drops line
-    // l % 4 of segment m = l / 4 (mod 8) if the 128-byte line lies wholly in
-    // that segment.  The barrier and release store that publish the slice
-    // come after, so the owner's all-gather write, which waits on a chain of
-    // progress words that starts there, is ordered after the discard.
-    __syncwarp();
-    const int lane = threadIdx.x & 31;
-    const uintptr_t end = reinterpret_cast<uintptr_t>(s4 + vhi);
-    for (long long s0 = vlo + 32ll * (threadIdx.x >> 5) + (long long)(lane >> 2) * T; s0 < vhi; s0 += 8ll * T) {
-        const uintptr_t seg = reinterpret_cast<uintptr_t>(s4 + s0);
-        const uintptr_t line = ((seg + 127) & ~(uintptr_t)127) + 128u * (unsigned)(lane & 3);
-        const uintptr_t seg_end = seg + 512 < end ? seg + 512 : end;
-        if (line + 128 <= seg_end) asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
-    }
+    // all-gather step, and nobody reads it before that.  Drop its lines from
+    // L2 so that a partial still there is never written back.
+    if (discard_src) discard_read_lines(s4, vlo, vhi, T);
 }
 
 template <int DT, int OP, bool VEC>
@@ -172,10 +156,15 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
     // contribution once, where it enters the reduction
     const bool scale_here = OP == OP_AVG && a.layout != RING_INTRA;
     const bool prediv_here = OP == OP_AVG_PREDIV && a.layout != RING_INTER;
-    // a launch of the whole flat schedule overwrites every partial it hands
-    // over with the chunk's final value before it ends: the receiver drops
-    // the partial's lines from L2 once read (ring_slice)
-    const bool discard_partials = a.layout == RING_FLAT && a.first_step == 0 && a.n_steps == 2 * (rp - 1);
+    // the receiver drops a partial's lines from L2 once read (ring_slice)
+    // where the partial is certain to be overwritten before anyone reads it
+    // again: a launch of the whole flat or across-node schedule (its own
+    // all-gather), and the hierarchical schedule's reduce-scatter inside the
+    // nodes (its all-gather launch); not a reduce-scatter call, whose
+    // result includes the partials
+    const bool discard_partials =
+        (a.layout != RING_INTRA && a.first_step == 0 && a.n_steps == 2 * (rp - 1)) ||
+        (a.layout == RING_INTRA && a.first_step == 0);
     const char *src = rank_ptr(a.bufs, p, nb);
     char *dst = rank_ptr(a.bufs, p, r);
     unsigned long long *my_flag = a.flags + blockIdx.x;

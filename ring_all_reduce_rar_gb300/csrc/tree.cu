@@ -28,10 +28,12 @@ namespace rar {
 constexpr int kTreeThreads = 512;
 
 // One slice [lo, hi): reduce: dst = op(dst, src) (+ the root's avg scaling);
-// broadcast: dst = src.
+// broadcast: dst = src.  discard_src: src is a child's partial that nobody
+// reads again before the broadcast overwrites it; its lines are dropped
+// from L2 once read, so that it is not written back.
 template <int DT, int OP, bool VEC>
 __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
-                                           bool scale, float inv_p) {
+                                           bool scale, bool discard_src, float inv_p) {
     constexpr int hop_op = HopOf<OP>::value;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
     const int T = blockDim.x;
@@ -56,6 +58,7 @@ __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long
         if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
         d4[v] = x;
     }
+    if (discard_src) discard_read_lines(s4, vlo, vhi, T);
 }
 
 template <int DT, int OP, bool VEC>
@@ -131,7 +134,8 @@ __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __
                 if (s_stop) goto done;
                 const long long lo = sl * a.slice;
                 const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
-                tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, up && r == 0 && l == L - 1, a.inv_p);
+                // from level 1 up the child holds a partial sum of its subtree
+                tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, up && r == 0 && l == L - 1, up && l > 0, a.inv_p);
                 __syncthreads();
                 if (threadIdx.x == 0) atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // the peer sent
             }

@@ -9,9 +9,10 @@
 // sender's copy in place), so a reduce-scatter hop costs 3 element moves
 // (read incoming, read own, write own) and an all-gather hop 2.  A partial
 // that has been handed on is dead until its owner's all-gather step
-// overwrites it, so in a launch of the whole schedule the receiver drops
-// its lines from L2 once it has read them: a partial still in L2 then never
-// reaches DRAM.
+// overwrites it, so where that overwrite is certain -- a launch of the whole
+// flat or cross-node schedule, and the hierarchical reduce-scatter inside
+// the nodes, whose all-gather launch follows -- the receiver drops its lines
+// from L2 once it has read them: a partial still in L2 never reaches DRAM.
 //
 // Pipelining ("What real libraries add", "Pipelining"): each chunk is cut
 // into slices of `slice` elements; slice k belongs to channel k mod
@@ -31,7 +32,9 @@
 // rank r - 1 overwrites the slice r read at reduce-scatter step s only at its
 // all-gather step s, and that write waits on a chain of flags that starts
 // with r's own release after the read (the chunk's remaining reduce-scatter
-// hops, its owner, the all-gather hops up to r - 1).
+// hops, its owner, the all-gather hops up to r - 1).  The same chain orders
+// that write after r's discard of the slice's lines, which r issues before
+// its release (PTX treats a discard as a write of an indeterminate value).
 //
 // Bidirectional variant ("Bidirectional rings"): channels
 // [fwd_channels, channels) run the mirrored ring (send to r - 1) on the

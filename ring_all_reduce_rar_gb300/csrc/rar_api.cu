@@ -472,19 +472,23 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         if (path == 0)
             path = (stream_ok && (size_t)p * bytes >= (size_t)256 << 20 && bytes >= (size_t)8 << 20) ? 2 : 1;
         if (path == 2) {
-            // tile per rank: slice_elems, else the largest tile up to 32 KB
-            // (a multiple of 512 bytes) that cuts the buffer into k rounds of
-            // one tile per CTA (one CTA per SM), k >= 4, with the last round
-            // nearly full; stages: channels, else 3
+            // tile per rank: slice_elems (up to 32 KB), else the largest tile
+            // up to 28 KB (a multiple of 512 bytes) that cuts the buffer into
+            // k rounds of one tile per CTA (one CTA per SM), k >= 4, with the
+            // last round nearly full; stages: channels, else 3.  (28 KB
+            // against 32 KB tiles on GB300: p = 8 bf16 at 16 GiB 5.10 / 5.20
+            // ms, p = 16 int32 at 256 MB per rank 1.27 / 1.31 ms, p = 4 and
+            // p = 64 equal; 24 KB fell to 0.93 of the roofline at p = 4.)
             size_t tb;
             if (h->opt.slice_elems) {
                 tb = (size_t)h->opt.slice_elems * (size_t)elem_bytes(dtype);
                 tb = std::min<size_t>(std::max<size_t>(tb / 512 * 512, 512), 32768);
             } else {
+                constexpr size_t kAutoTile = 28672;
                 const size_t sms = (size_t)h->sm_count;
-                const size_t rounds = std::max<size_t>(4, (bytes + 32768 * sms - 1) / (32768 * sms));
+                const size_t rounds = std::max<size_t>(4, (bytes + kAutoTile * sms - 1) / (kAutoTile * sms));
                 tb = (bytes + rounds * sms - 1) / (rounds * sms);
-                tb = std::min<size_t>(std::max<size_t>((tb + 511) / 512 * 512, 512), 32768);
+                tb = std::min<size_t>(std::max<size_t>((tb + 511) / 512 * 512, 512), kAutoTile);
             }
             const int stages = h->opt.channels ? h->opt.channels : 3;
             if (stages < 2 || stages > 8 || (size_t)(stages + 2) * tb > 227 * 1024)

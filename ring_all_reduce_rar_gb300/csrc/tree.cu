@@ -43,22 +43,26 @@ __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long
         if (OP == OP_AVG && scale) x = scale_word<DT>(x, inv_p);
         store_elem<DT>(dst, i, x);
     };
-    long long vlo = (lo + VE - 1) / VE, vhi = hi / VE;
-    if (!VEC || vlo >= vhi) {
+    if constexpr (!VEC) {
         for (long long i = lo + threadIdx.x; i < hi; i += T) one(i);
-        return;
+    } else {
+        const long long vlo = (lo + VE - 1) / VE, vhi = hi / VE;
+        if (vlo >= vhi) {
+            for (long long i = lo + threadIdx.x; i < hi; i += T) one(i);
+            return;
+        }
+        for (long long i = lo + threadIdx.x; i < vlo * VE; i += T) one(i);
+        for (long long i = vhi * VE + threadIdx.x; i < hi; i += T) one(i);
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+        for (long long v = vlo + threadIdx.x; v < vhi; v += T) {
+            uint4 x = __ldcg(s4 + v);
+            if (reduce) x = hop_vec<DT, hop_op>(__ldcs(d4 + v), x);
+            if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
+            d4[v] = x;
+        }
+        if (discard_src) discard_read_lines(s4, vlo, vhi, T);
     }
-    for (long long i = lo + threadIdx.x; i < vlo * VE; i += T) one(i);
-    for (long long i = vhi * VE + threadIdx.x; i < hi; i += T) one(i);
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-    for (long long v = vlo + threadIdx.x; v < vhi; v += T) {
-        uint4 x = __ldcg(s4 + v);
-        if (reduce) x = hop_vec<DT, hop_op>(__ldcs(d4 + v), x);
-        if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
-        d4[v] = x;
-    }
-    if (discard_src) discard_read_lines(s4, vlo, vhi, T);
 }
 
 template <int DT, int OP, bool VEC>

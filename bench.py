@@ -5,7 +5,7 @@ elements) by the engine under test.  The headline workload is p = 8 virtual
 ranks, N = 2^30 bf16 elements per rank (16 GiB in total, far above the
 129 MB L2, so no flush is needed between steps), op = sum.
 
-    python bench.py [--steps K] [--warmup W] [--engine fused|ring|ring_bidir|all]
+    python bench.py [--steps K] [--warmup W] [--engine fused|ring|ring_bidir|tree|all]
     python bench.py --impl reference      # the CPU oracle on the host cores
     python bench.py --sweep [--pair 0|1|2] # p = 16, N = 4^5 ... 4^13, every engine
     python bench.py --configs             # every workload on every engine
@@ -15,8 +15,8 @@ ranks, N = 2^30 bf16 elements per rank (16 GiB in total, far above the
 Metric: algBW = p * N * element bytes / time per step (GB/s), summed over
 GPUs when run under torchrun (independent replicas, weak scaling).  Also
 reported: each engine's fraction of the HBM roofline, with the roofline
-bytes 2 p N e (fused) and 5 (p - 1) N e (ring), against the measured copy
-bandwidth in MEASURED_PEAKS.json.
+bytes 2 p N e (fused) and 5 (p - 1) N e (ring and tree executors), against
+the measured copy bandwidth in MEASURED_PEAKS.json.
 """
 from __future__ import annotations
 
@@ -278,7 +278,7 @@ def run_ours(args):
     seed = w.seed_of(cfg["index"]) + 1000 * ctx.rank
     big, rows = w.make_inputs(p, n, dtype, cfg["dist"], seed, device=dev)
     torch.cuda.synchronize()
-    engines = ["fused", "ring", "ring_bidir"] if args.engine == "all" else [args.engine]
+    engines = ["fused", "ring", "ring_bidir", "tree"] if args.engine == "all" else [args.engine]
     peak, peak_kind = hbm_peak()
     results = {}
     with ClockSampler(ctx.local_rank) as clk:

@@ -111,7 +111,7 @@ typedef enum {
     RAR_EUNSUPPORTED = 2,  /* valid but not offered (avg on int32, grid not co-resident) */
     RAR_ENOMEM = 3,        /* scratch allocation failed in rar_init */
     RAR_ECUDA = 4,         /* a CUDA runtime call failed; message in rar_last_error */
-    RAR_ETIMEOUT = 5,      /* a ring wait ran past timeout_ns (from rar_status) */
+    RAR_ETIMEOUT = 5,      /* a bounded wait ran past timeout_ns (from rar_status) */
     RAR_EABORTED = 6       /* the call was abandoned after another CTA timed out */
 } rar_status_code;
 
@@ -123,9 +123,19 @@ typedef struct {
     int channels;                  /* ring engines: CTAs per rank, 0 = chosen from the SM count */
     int slice_elems;               /* ring engines: elements per pipelined slice, 0 = auto */
     int block_threads;             /* threads per CTA (multiple of 32, <= 1024), 0 = auto */
-    unsigned long long timeout_ns; /* ring engines: bound on every wait, 0 = 2 s */
+    unsigned long long timeout_ns; /* bound on every wait of the ring and tree engines and
+                                      of the fused engine's streaming path (a bulk load
+                                      that does not arrive); 0 = 2 s; nonzero values
+                                      below 1 ms (1000000) are refused with RAR_EINVAL.
+                                      A wait that runs out ends the call with
+                                      RAR_ETIMEOUT (rar_status); the streaming path
+                                      still waits for every bulk load it issued before
+                                      its CTAs finish, whatever this bound */
     int skip_pointer_check;        /* nonzero: skip the per-call device-pointer query */
-    int fault_mode;                /* rar_fault_mode, ring engines only (tests) */
+    int fault_mode;                /* rar_fault_mode (tests): ring and tree engines; and
+                                      RAR_FAULT_MUTE on the fused streaming path, where
+                                      the loads of rank fault_rank are never issued, as
+                                      if that rank had died */
     int fault_rank;                /* rank the fault applies to */
     unsigned fault_delay_ns;       /* RAR_FAULT_DELAY: pause before each slice */
     int fused_path;                /* RAR_ENGINE_FUSED data path, same results on both:
@@ -244,17 +254,23 @@ int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bu
  * allocator, a pre-planned arena with a fixed budget), and callers that
  * cannot pay for cudaMalloc/cudaFree at call time (both can block; cudaFree
  * synchronises the device).  The source pages have no counterpart: this is
- * the ring executor (RAR_ENGINE_RING, default tuning) without a handle,
+ * the ring executor (RAR_ENGINE_RING with progress words) without a handle,
  * with its scratch -- progress words, receive counters, the status and the
  * abort word -- in one fixed-size device array inside the library (about
- * 16 KB, resident on every GPU that loads the library until exit).
+ * 16 KB, resident on every GPU that loads the library until exit).  Its
+ * tuning is fixed: 256 threads per CTA, every co-resident CTA up to 1024 in
+ * all, 128 KB slices (the handle's ring uses 512 threads and slices of up to
+ * 128 KB); the results are the same bits as rar_allreduce's with
+ * RAR_ENGINE_RING.
  * Arguments and results are as rar_allreduce's, on the current device.
  * Limits: p <= 64 and p * channels <= 1024 CTAs; larger p returns
  * RAR_EINVAL with a message from rar_last_error(NULL).
  * The first call on a device, with that device current, sets the array up
- * (takes its address and clears it once); make that first call before any
- * stream capture.  Every call uses the same array: calls that overlap on
- * the GPU (two streams, two threads) race and must be ordered by the caller.
+ * (clears it once, synchronously; so does the first call after
+ * cudaDeviceReset, which reloads the array); make that first call before
+ * any stream capture.  Every call uses the same array: calls that overlap
+ * on the GPU (two streams, two threads) race and must be ordered by the
+ * caller.
  * A ring wait that runs out (2 s) ends the kernel early and leaves the
  * buffers partly reduced; without a handle this entry point cannot report
  * it, so callers who need that status use rar_allreduce.

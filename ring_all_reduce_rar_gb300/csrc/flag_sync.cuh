@@ -106,6 +106,13 @@ __device__ __forceinline__ void launch_epoch_end(const RingArgs &a, unsigned epo
     if (epoch == 0xFFFFFFFFu) {
         for (int i = threadIdx.x; i < a.flag_capacity; i += blockDim.x) a.flags[i] = 0ull;
         for (long long i = threadIdx.x; i < a.mailbox_words; i += blockDim.x) a.mailbox[i] = 0ull;
+        // the abort word and the status's first-reporter epoch only grow
+        // (atomicMax) within a count: a stale value would abort the launch
+        // that reaches it again after the wrap, or hide its timeout details
+        if (threadIdx.x == 0) {
+            *a.abort_word = 0u;
+            a.status->epoch = 0u;
+        }
         __syncthreads();
     }
     if (threadIdx.x == 0) {

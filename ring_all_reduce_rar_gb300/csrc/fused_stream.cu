@@ -24,9 +24,21 @@
 // ring of shared-memory stages (full/empty mbarriers); eight consumer warps
 // fold.  The result of a tile goes to a double-buffered shared-memory row,
 // and its p cp.async.bulk stores are issued one per step of the next tile,
-// interleaved with that tile's loads.  All waits are bounded; one that runs
-// out records RAR_ETIMEOUT and the CTA drains its own copies (bounded) and
-// returns.
+// interleaved with that tile's loads.
+//
+// Failure path.  A consumer warp's wait for a stage is bounded by the call's
+// timeout; one that runs out records RAR_ETIMEOUT (with the rank whose tile
+// never arrived) and raises a shared flag, and from then on no consumer
+// releases a stage: a stage is handed back only after its load was seen
+// complete, so the producer never reissues into a stage with a load still in
+// flight.  The producer's wait for a free stage gives up on the same flag or
+// timeout.  Before the producer -- and with it the CTA -- finishes, it waits
+// for every bulk load it issued, whatever the call's timeout: an issued load
+// always completes, so that wait ends by itself; it still has its own fixed
+// limit (kStreamDrainLimitNs), far beyond any load's latency.  Bulk stores
+// are waited for with cp.async.bulk.wait_group.  A host-requested fault
+// (RAR_FAULT_MUTE) makes the producer stop issuing at the first load of the
+// muted rank, so the consumers' bounded waits run out as for a dead rank.
 #include "fused_impl.cuh"
 
 namespace rar {
@@ -85,15 +97,31 @@ __device__ __forceinline__ unsigned long long st_global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-__device__ __forceinline__ bool st_mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+// Wait for the phase of `bar` with this parity; false once `timeout_ns`
+// passed (globaltimer, with an iteration cap) or `*stop` became nonzero.
+__device__ __forceinline__ bool st_mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+                                                     const volatile int *stop) {
     if (st_mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = st_global_ns();
     const unsigned long long max_iters = timeout_ns / 16ull + (1ull << 20);
     for (unsigned long long it = 0; it < max_iters; it++) {
         if (st_mbar_try_wait(bar, parity)) return true;
-        if ((it & 255) == 0 && st_global_ns() - t0 > timeout_ns) return false;
+        if ((it & 63) == 63 && (*stop || st_global_ns() - t0 > timeout_ns)) return false;
     }
     return false;
+}
+
+// The producer's wait for a bulk load it issued itself.  It does not take
+// the call's timeout: the load completes by itself, and the CTA must not
+// finish while it can still write shared memory.  The fixed limit only
+// guards against a broken device.
+constexpr unsigned long long kStreamDrainLimitNs = 10000000000ull;  // 10 s
+__device__ __forceinline__ void st_mbar_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = st_global_ns();
+    for (unsigned long long it = 0; it < (1ull << 36); it++) {
+        if (st_mbar_try_wait(bar, parity)) return;
+        if ((it & 255) == 255 && st_global_ns() - t0 > kStreamDrainLimitNs) return;
+    }
 }
 
 // A vector across a chunk boundary (at most p - 1 in a buffer): each lane is
@@ -124,7 +152,9 @@ template <int DT, int OP, int VPT>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     fused_stream_kernel(const __grid_constant__ FusedArgs a, int tile_bytes, int n_stages) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_fail;
+    __shared__ int s_fail;  // a consumer warp's wait ran out (then s_fail_* say where)
+    __shared__ int s_fail_rank, s_fail_step;
+    __shared__ long long s_fail_tile;
     constexpr int EB = ElemInfo<DT>::bytes;
     constexpr int VE = 16 / EB;
     constexpr int hop_op = HopOf<OP>::value;
@@ -167,7 +197,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     if (warp == 0) {
         // ---- producer: one bulk load per step, into the next free stage
         if (lane != 0) return;
-        long long g = 0;
+        const int muted_rank = a.fault_mode == RAR_FAULT_MUTE ? a.fault_rank : -1;
+        long long g = 0;  // loads issued
         bool ok = true;
         for (long long k = 0; k < my_tiles && ok; k++) {
             const long long off = tile_off(k);
@@ -177,20 +208,29 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             for (int j = 0; j < steps; j++, g++) {
                 const int s = (int)(g % NS);
                 const long long use = g / NS;
-                if (use > 0 && !st_mbar_wait_bounded(st_smem_addr(&empty[s]), (uint32_t)((use - 1) & 1), a.timeout_ns)) {
-                    ok = false;  // the consumers stopped (they record why)
+                // a stage comes back only once all consumer warps saw its
+                // previous load complete; give up when they stopped
+                if (use > 0 &&
+                    !st_mbar_wait_bounded(st_smem_addr(&empty[s]), (uint32_t)((use - 1) & 1), a.timeout_ns, &s_fail)) {
+                    ok = false;
+                    break;
+                }
+                const int rank = (c0 + j) % p;
+                if (rank == muted_rank) {  // injected dead rank: its data never comes
+                    ok = false;
                     break;
                 }
                 st_fence_proxy_async();
                 const uint32_t bar = st_smem_addr(&full[s]);
                 st_mbar_expect_tx(bar, bytes);
-                st_bulk_load(st_smem_addr(stage + (size_t)s * TB), rank_ptr(a.bufs, p, (c0 + j) % p) + off, bytes, bar);
+                st_bulk_load(st_smem_addr(stage + (size_t)s * TB), rank_ptr(a.bufs, p, rank) + off, bytes, bar);
             }
         }
-        // loads still in flight land in this CTA's shared memory: wait for
-        // them (bounded) before this thread, and with it the CTA, can finish
+        // Every load before the last NS was seen complete by the consumers
+        // (its stage came back); the last NS may still be writing this CTA's
+        // shared memory, so wait for each of them before finishing.
         for (long long h = g - NS > 0 ? g - NS : 0; h < g; h++)
-            st_mbar_wait_bounded(st_smem_addr(&full[h % NS]), (uint32_t)((h / NS) & 1), a.timeout_ns);
+            st_mbar_drain(st_smem_addr(&full[h % NS]), (uint32_t)((h / NS) & 1));
         return;
     }
 
@@ -235,10 +275,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         for (int j = 0; j < steps; j++, g++) {
             const int s = (int)(g % NS);
             if (!failed) {
-                if (*(volatile int *)&s_fail || !st_mbar_wait_bounded(st_smem_addr(&full[s]), (uint32_t)((g / NS) & 1),
-                                                                       a.timeout_ns)) {
+                // warp-uniform: the warp goes on only if every lane saw the load
+                bool ok = !*(volatile int *)&s_fail &&
+                          st_mbar_wait_bounded(st_smem_addr(&full[s]), (uint32_t)((g / NS) & 1), a.timeout_ns, &s_fail);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
                     failed = true;
-                    s_fail = 1;
+                    if (lane == 0 && atomicCAS(&s_fail, 0, 1) == 0) {  // the first to fail records where
+                        s_fail_rank = (c0 + j) % p;
+                        s_fail_step = j;
+                        s_fail_tile = blockIdx.x + k * gridDim.x;
+                    }
                 }
             }
             if (!failed) {
@@ -256,8 +303,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
             }
             __syncwarp();
-            if (lane == 0) st_mbar_arrive(st_smem_addr(&empty[s]));  // this warp is done with the stage
-            if (ct == 0) issue_pending_store();
+            if (!failed) {
+                // this warp is done with the stage, whose load it saw complete
+                if (lane == 0) st_mbar_arrive(st_smem_addr(&empty[s]));
+                if (ct == 0) issue_pending_store();
+            }
         }
 
         // tile end: result row (double-buffered), then p bulk stores
@@ -293,13 +343,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
     }
 
-    if (failed || *(volatile int *)&s_fail) {
+    if (failed) {
+        // (s_fail_* were written before the barrier that ended the tile)
         if (ct == 0) {
             a.status->code = RAR_ETIMEOUT;
-            a.status->rank = -1;
-            a.status->step = -1;
-            a.status->slice = (int)(blockIdx.x + k * gridDim.x);
-            a.status->waited_on = -1;
+            a.status->rank = -1;  // no rank group: a tile of the fused engine
+            a.status->step = s_fail_step;
+            a.status->slice = (int)s_fail_tile;
+            a.status->waited_on = s_fail_rank;
             a.status->flag_seen = 0;
             a.status->flag_wanted = 0;
             __threadfence();

@@ -17,6 +17,11 @@ using namespace rar;
 constexpr int kMaxRingCtas = 8192;           // flags / counters capacity
 constexpr int kRingPhases = 3;               // counter arrays: one per ring launch of a call
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+// Shortest accepted rar_options.timeout_ns: a bound on waits of a few
+// microseconds (a hand-off, a bulk load) that still leaves headroom for a
+// preempted or briefly stalled CTA; shorter values would report timeouts of
+// healthy launches.
+constexpr unsigned long long kMinTimeoutNs = 1000000ull;
 constexpr long long kMaxSlicesPerChannelStep = (1ll << 20) - 2;  // slice positions per channel and step
 constexpr long long kRingMaxSliceBytes = 128 << 10;
 constexpr long long kLLMailboxWords = (long long)RAR_LL_MAILBOX_BYTES / 8;
@@ -104,6 +109,8 @@ int check_options(rar_ctx *h, const rar_options &o) {
     if (o.hier_group < 0 || o.hier_group > RAR_MAX_P) return fail(h, RAR_EINVAL, "hier_group out of range");
     if (o.protocol < 0 || o.protocol > 2) return fail(h, RAR_EINVAL, "unknown protocol");
     if (o.slice_block < 0) return fail(h, RAR_EINVAL, "negative slice_block");
+    if (o.timeout_ns != 0 && o.timeout_ns < kMinTimeoutNs)
+        return fail(h, RAR_EINVAL, "timeout_ns must be 0 (2 s) or at least 1 ms (1000000)");
     return RAR_OK;
 }
 
@@ -445,6 +452,8 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         a.inv_p = inv_p;
         a.status = h->status;
         a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
+        a.fault_mode = h->opt.fault_mode;
+        a.fault_rank = h->opt.fault_rank;
         const bool tree = engine == RAR_ENGINE_FUSED_TREE && phase != PHASE_AG;
         if (hier) {
             if (engine != RAR_ENGINE_FUSED || phase != PHASE_ALL || h->opt.fused_path == 2)
@@ -577,6 +586,9 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
     g_init_error.clear();
     if (!out) return fail(nullptr, RAR_EINVAL, "out is NULL");
     *out = nullptr;
+    rar_options o{};
+    if (opt) o = *opt;
+    if (check_options(nullptr, o) != RAR_OK) return RAR_EINVAL;
     int ndev = 0;
     cudaError_t ce = cudaGetDeviceCount(&ndev);
     if (ce != cudaSuccess) {
@@ -584,9 +596,6 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
         return fail(nullptr, RAR_ECUDA, std::string("cudaGetDeviceCount: ") + cudaGetErrorString(ce));
     }
     if (device < 0 || device >= ndev) return fail(nullptr, RAR_EINVAL, "no such device");
-    rar_options o{};
-    if (opt) o = *opt;
-    if (check_options(nullptr, o) != RAR_OK) return RAR_EINVAL;
 
     rar_ctx *h = new rar_ctx();
     h->device = device;
@@ -731,7 +740,10 @@ int rar_status(rar_handle h) {
                           "(progress word 0x%llx, wanted 0x%llx)",
                           st.rank, st.step, st.slice, st.waited_on, st.flag_seen, st.flag_wanted);
         else
-            std::snprintf(buf, sizeof(buf), "bulk-copy wait timed out on tile %d", st.slice);
+            std::snprintf(buf, sizeof(buf),
+                          "bulk-copy wait timed out: tile %d, step %d, waiting for rank %d's tile (fused streaming "
+                          "path)",
+                          st.slice, st.step, st.waited_on);
         h->err = buf;
         return st.code ? (int)st.code : RAR_ETIMEOUT;
     }

@@ -82,9 +82,13 @@ struct FusedArgs {
     int p;
     int phase;     // Phase
     float inv_p;   // binary32 nearest to 1/p
-    // streaming path only: where a bounded wait that ran out is recorded
+    // streaming path only: where a bounded wait that ran out is recorded,
+    // the bound, and the host-requested fault (RAR_FAULT_MUTE: the loads of
+    // rank fault_rank are never issued)
     RingStatus *status;
     unsigned long long timeout_ns;
+    int fault_mode;
+    int fault_rank;
 };
 
 // Which rings a ring launch runs (the hierarchical schedule uses 1 and 2).

@@ -105,3 +105,25 @@ def test_python_binding_refuses_cpu_tensors(lib):
         rar._abi._marshal([torch.zeros(4), torch.zeros(4)])
     with pytest.raises(ValueError):
         rar._abi._marshal([])
+
+
+def test_short_timeouts_are_refused_before_any_device_work(lib):
+    """timeout_ns bounds every wait of the ring and tree executors and of the
+    fused streaming path; a nonzero bound under 1 ms is refused by rar_init
+    (argument checks come before the device is touched, so this holds on a
+    machine without a GPU too)."""
+    for bad in (1, 999_999):
+        o = rar.make_options(engine="fused", timeout_ns=bad)
+        h = ctypes.c_void_p()
+        assert lib.rar_init(ctypes.byref(h), 0, ctypes.byref(o)) == 1  # RAR_EINVAL
+        assert h.value is None
+        assert "timeout_ns" in rar.rar_last_error(None)
+    o = rar.make_options(engine="ring", timeout_ns=1_000_000)
+    h = ctypes.c_void_p()
+    rc = lib.rar_init(ctypes.byref(h), 0, ctypes.byref(o))
+    import torch
+    if torch.cuda.is_available():
+        assert rc == 0
+        lib.rar_destroy(h)
+    else:
+        assert rc in (1, 4) and "timeout_ns" not in rar.rar_last_error(None)

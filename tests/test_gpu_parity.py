@@ -433,6 +433,55 @@ def test_ring_muted_rank_times_out_and_handle_recovers(rar, dev, engine):
         assert_bits_equal(rows, ref, "after timeout")
 
 
+@pytest.mark.parametrize("p,n", [(4, 4 * 65536 + 12), (8, 8 * 40000 + 8)])
+def test_fused_stream_muted_rank_times_out_and_handle_recovers(rar, dev, p, n):
+    """The fused streaming path with a dead rank (RAR_FAULT_MUTE: its bulk
+    loads are never issued): the consumers' bounded waits run out, the call
+    reports RAR_ETIMEOUT naming that rank, every CTA finishes (the producer
+    waits for the loads it did issue), and the next call on the same handle
+    is exact ("Ring All-Reduce, in depth", "Failure modes": a dead rank must
+    end in an error, not a hang)."""
+    host = gen(p, n, "bfloat16", ("normal", 1e-2), 31 + p)
+    ref, _ = oracle_expect(host, "bfloat16", "sum", "fused")
+    _, rows = upload(host, dev)
+    with rar.Handle(0, engine="fused", fused_path="stream", timeout_ns=50_000_000, fault_mode="mute",
+                    fault_rank=p - 2) as h:
+        h.allreduce(rows)
+        assert h.status() == 5  # RAR_ETIMEOUT
+        msg = rar.rar_last_error(h.h)
+        assert "bulk-copy wait timed out" in msg and f"waiting for rank {p - 2}'s tile" in msg, msg
+        assert h.status() == 0  # each failure is reported once
+        h.set_options(engine="fused", fused_path="stream", timeout_ns=50_000_000)
+        for _ in range(2):
+            _, rows = upload(host, dev)
+            h.allreduce(rows)
+            h.check()
+            assert_bits_equal(rows, ref, "fused stream after timeout")
+
+
+@pytest.mark.parametrize("engine", ["ring", "ring_ll", "ring_bidir", "tree", "tree_ll"])
+def test_epoch_wrap_after_a_timeout(rar, dev, engine):
+    """A timed-out launch at epoch E raises the abort word to E.  The launch
+    that wraps the 32-bit epoch clears it, so that the launch that reaches
+    epoch E again after the wrap runs normally instead of taking itself for
+    aborted."""
+    E = 3
+    host = gen(8, 8 * 3000 + 5, "bfloat16", ("normal", 1e-2), 91)
+    ref, _ = oracle_expect(host, "bfloat16", "sum", engine)
+    with rar.Handle(0, **handle_opts(engine, timeout_ns=50_000_000, fault_mode="mute", fault_rank=2)) as h:
+        rar.rar_debug_set_epoch(h.h, E - 1)
+        _, rows = upload(host, dev)
+        h.allreduce(rows)  # runs with epoch E, times out
+        assert h.status() == 5
+        h.set_options(**handle_opts(engine, timeout_ns=50_000_000))
+        rar.rar_debug_set_epoch(h.h, 0xFFFFFFFE)
+        for k in range(E + 1):  # epochs 0xFFFFFFFF (the wrap), 1, ..., E
+            _, rows = upload(host, dev)
+            h.allreduce(rows)
+            h.check()
+            assert_bits_equal(rows, ref, f"{engine}: call {k} after the wrap")
+
+
 @pytest.mark.parametrize("engine", ["ring", "ring_ll", "ring_bidir", "tree", "tree_ll"])
 def test_epoch_wrap_around(rar, dev, engine):
     """Progress and mailbox words carry a 32-bit launch epoch.  The launch

@@ -19,9 +19,14 @@
 // The array is about 16 KB and stays resident on every GPU that loads the
 // library until the process exits.
 //
-// Set-up: the first call on a device (with that device current) takes the
-// array's device address with cudaGetSymbolAddress and clears the array
-// once; make that first call before any stream capture.
+// Set-up: every call takes the array's device address on the current device
+// with cudaGetSymbolAddress (cheap; it allocates nothing).  The first call
+// on a device, and the first after the array moved (the module is loaded
+// again after cudaDeviceReset), also clears the array once, synchronously;
+// make that first call before any stream capture.
+// Tuning, fixed: 256 threads per CTA, every co-resident CTA up to 1024 in
+// all (p * channels), slices of 128 KB, one slice position at a time through
+// every step.  The results do not depend on it.
 // Every call shares the array: progress words carry the launch's epoch (kept
 // in the array itself), so no per-call clearing is needed, but two calls
 // that overlap on the GPU (on two streams, or from two threads) race on the
@@ -59,8 +64,7 @@ constexpr size_t kScratchWords = (sizeof(NoAllocScratch) + 7) / 8;
 static __device__ __align__(256) unsigned long long g_noalloc_scratch[kScratchWords];
 
 struct DeviceSlot {
-    bool ready = false;
-    NoAllocScratch *scratch = nullptr;  // device address of g_noalloc_scratch
+    void *cleared = nullptr;  // the array's device address when it was last cleared
 };
 
 std::mutex g_mutex;
@@ -119,24 +123,28 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     const int G = max_ctas / p;
     if (G < 1) return reject(RAR_EUNSUPPORTED, "p rank groups cannot be co-resident");
 
-    NoAllocScratch *scratch = nullptr;
+    // The array's address on this device.  In host code the symbol is only a
+    // host-side stand-in; the kernel must be given this address.
+    void *addr = nullptr;
+    ce = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return reject(RAR_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(ce));
+    }
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         DeviceSlot &slot = g_slots[dev];
-        if (!slot.ready) {
-            void *addr = nullptr;
-            ce = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
-            if (ce != cudaSuccess)
-                return reject(RAR_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(ce));
+        if (slot.cleared != addr) {
+            // first use of this copy of the array: start from zero (epoch,
+            // finish count, abort word, progress words)
             ce = cudaMemset(addr, 0, sizeof(g_noalloc_scratch));
             if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
             if (ce != cudaSuccess)
                 return reject(RAR_ECUDA, std::string("clearing the scratch array: ") + cudaGetErrorString(ce));
-            slot.scratch = static_cast<NoAllocScratch *>(addr);
-            slot.ready = true;
+            slot.cleared = addr;
         }
-        scratch = slot.scratch;
     }
+    NoAllocScratch *scratch = static_cast<NoAllocScratch *>(addr);
 
     // slices: at most 128 KB, and at most 2^20 - 2 slice positions per
     // channel and step (the progress words count 32-bit items)

@@ -570,3 +570,53 @@ def test_trivial_cases():
     np.testing.assert_array_equal(b[0], np.arange(5, dtype=np.float32))
     e = [np.zeros(0, dtype=np.float32) for _ in range(4)]
     assert list(oracle.simulate(e, "float32", "sum")) == [0, 0, 0, 0]
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "float16"])
+def test_f64_sum_against_fsum(dtype):
+    """orc_f64_sum, the fp64 reference behind the tree-order error bound:
+    per element, the sum over ranks and the sum of magnitudes, accumulated
+    in binary64.  Pinned against math.fsum (the correctly rounded sum) on
+    mixed-sign inputs spanning many binades: a sequential binary64 sum is
+    within (p - 1) 2^-53 sum|x| of it, which a binary32 accumulation, a
+    dropped rank or a missing abs in the magnitudes would all exceed."""
+    import math
+    rng = np.random.default_rng(20261202)
+    for p, n in [(2, 64), (7, 333), (64, 256)]:
+        # magnitudes from 2^-10 to 2^10, random signs
+        vals = rng.uniform(-1.0, 1.0, size=(p, n)) * np.exp2(rng.integers(-10, 11, size=(p, n)))
+        if dtype == "float32":
+            bufs = [v.astype(np.float32) for v in vals]
+            as64 = np.stack([b.astype(np.float64) for b in bufs])
+        else:
+            conv = oracle.f32_to_bf16 if dtype == "bfloat16" else oracle.f32_to_f16
+            back = oracle.bf16_to_f32 if dtype == "bfloat16" else oracle.f16_to_f32
+            bufs = [np.array([conv(float(x)) for x in v], dtype=np.uint16) for v in vals]
+            as64 = np.stack([[back(int(h)) for h in b] for b in bufs]).astype(np.float64)
+        ref, mag = oracle.f64_sum(bufs, dtype)
+        for i in range(n):
+            exact = math.fsum(as64[:, i])
+            exact_mag = math.fsum(np.abs(as64[:, i]))
+            bound = (p - 1) * 2.0 ** -53 * exact_mag
+            assert abs(ref[i] - exact) <= bound, (p, i)
+            assert abs(mag[i] - exact_mag) <= bound, (p, i)
+        # at least one element where binary32 accumulation is off by more
+        # than the bound (so the check above can tell the two apart)
+        f32 = np.zeros(n, dtype=np.float32)
+        for r in range(p):
+            f32 = (f32 + as64[r].astype(np.float32)).astype(np.float32)
+        exact_all = np.array([math.fsum(as64[:, i]) for i in range(n)])
+        mag_all = np.array([math.fsum(np.abs(as64[:, i])) for i in range(n)])
+        if p > 2:
+            assert np.any(np.abs(f32.astype(np.float64) - exact_all) > (p - 1) * 2.0 ** -53 * mag_all)
+
+
+def test_f64_sum_exact_cases():
+    """Integer-valued inputs: every partial sum is exact in binary64, so the
+    sum and the magnitudes equal the integer sums; a rank with value 0
+    everywhere and p = 1 included."""
+    for p in (1, 3, 16):
+        vals = [np.arange(-50, 50, dtype=np.float32) * (r - 1) for r in range(p)]
+        ref, mag = oracle.f64_sum([v.copy() for v in vals], "float32")
+        np.testing.assert_array_equal(ref, np.sum(np.stack(vals).astype(np.int64), axis=0).astype(np.float64))
+        np.testing.assert_array_equal(mag, np.sum(np.abs(np.stack(vals).astype(np.int64)), axis=0).astype(np.float64))

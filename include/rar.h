@@ -257,7 +257,7 @@ int rar_allreduce_host(rar_handle h, void *const *host_bufs, void *const *dev_bu
  * the ring executor (RAR_ENGINE_RING with progress words) without a handle,
  * with its scratch -- progress words, receive counters, the status and the
  * abort word -- in one fixed-size device array inside the library (about
- * 16 KB, resident on every GPU that loads the library until exit).  Its
+ * 80 KB, resident on every GPU that loads the library until exit).  Its
  * tuning is fixed: 256 threads per CTA, every co-resident CTA up to 1024 in
  * all, 128 KB slices (the handle's ring uses 512 threads and slices of up to
  * 128 KB); the results are the same bits as rar_allreduce's with

@@ -7,16 +7,17 @@
 //   - a caller that cannot pay for cudaMalloc/cudaFree at call time: both
 //     can block, and cudaFree synchronises the device.
 // rar_init allocates the ring executor's scratch.  This file offers the
-// same ring executor without a handle: its scratch -- one progress word and
-// one receive counter per CTA, the status word and the abort word -- lives
+// same ring executor without a handle: its scratch -- one progress word per
+// warp, one receive counter per CTA, the status word and the abort word -- lives
 // in one file-scope device array of fixed size, so the library allocates
 // nothing.  The caller still passes the rank buffers, which hold inputs and
 // outputs.
 //
 // Limits (checked on every call; anything beyond them is rejected):
 //   p <= 64 ranks (rank pointers travel in the kernel parameters), and
-//   p * channels <= 1024 CTAs (the array holds 1024 progress words).
-// The array is about 16 KB and stays resident on every GPU that loads the
+//   p * channels <= 1024 CTAs (the array holds a progress word for each of
+//   their warps).
+// The array is about 80 KB and stays resident on every GPU that loads the
 // library until the process exits.
 //
 // Set-up: every call takes the array's device address on the current device
@@ -52,7 +53,7 @@ constexpr unsigned long long kNoAllocTimeoutNs = 2000000000ull;
 
 // Layout of the scratch array.
 struct NoAllocScratch {
-    unsigned long long flags[kNoAllocMaxCtas];
+    unsigned long long flags[kNoAllocMaxCtas * (kNoAllocThreads / 32)];  // one per warp
     unsigned long long recv_counts[kNoAllocMaxCtas];
     RingStatus status;
     unsigned abort_word;
@@ -171,7 +172,7 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.inv_p = 1.0f / (float)p;
     a.epoch_word = &scratch->epoch_word;
     a.finish_count = &scratch->finish_count;
-    a.flag_capacity = kNoAllocMaxCtas;
+    a.flag_capacity = kNoAllocMaxCtas * (kNoAllocThreads / 32);
     a.flags = scratch->flags;
     a.mailbox = nullptr;
     a.mailbox_words = 0;

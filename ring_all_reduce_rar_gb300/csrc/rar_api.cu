@@ -14,7 +14,8 @@ namespace {
 
 using namespace rar;
 
-constexpr int kMaxRingCtas = 8192;           // flags / counters capacity
+constexpr int kMaxRingCtas = 8192;           // counters capacity; CTAs of a ring or tree launch
+constexpr int kFlagWords = kMaxRingCtas * kRingMaxWarps;  // progress words (one per ring warp)
 constexpr int kRingPhases = 3;               // counter arrays: one per ring launch of a call
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 // Shortest accepted rar_options.timeout_ns: a bound on waits of a few
@@ -208,7 +209,7 @@ RingArgs handle_ring_args(const rar_ctx *h, const RankPtrs &ptrs, int p, size_t 
     a.inv_p = 1.0f / (float)p;
     a.epoch_word = h->epoch_words;
     a.finish_count = h->epoch_words + 1;
-    a.flag_capacity = kMaxRingCtas;
+    a.flag_capacity = kFlagWords;
     a.flags = h->flags;
     a.mailbox = h->ll_box;
     a.mailbox_words = kLLMailboxWords;
@@ -610,7 +611,7 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
         delete h;
         return fail(nullptr, RAR_ECUDA, "querying the device's SM count failed");
     }
-    bool ok = cudaMalloc((void **)&h->flags, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+    bool ok = cudaMalloc((void **)&h->flags, sizeof(unsigned long long) * kFlagWords) == cudaSuccess &&
               cudaMalloc((void **)&h->recv_counts, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
               cudaMalloc((void **)&h->status, sizeof(RingStatus)) == cudaSuccess &&
               cudaMalloc((void **)&h->abort_word, sizeof(unsigned)) == cudaSuccess &&
@@ -618,7 +619,7 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
               cudaMalloc((void **)&h->ptr_table, sizeof(void *) * RAR_MAX_P) == cudaSuccess &&
               cudaMalloc((void **)&h->ll_box, sizeof(unsigned long long) * kLLMailboxWords) == cudaSuccess;
     if (ok) {
-        ok = cudaMemset(h->flags, 0, sizeof(unsigned long long) * kMaxRingCtas) == cudaSuccess &&
+        ok = cudaMemset(h->flags, 0, sizeof(unsigned long long) * kFlagWords) == cudaSuccess &&
              cudaMemset(h->recv_counts, 0, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
              cudaMemset(h->status, 0, sizeof(RingStatus)) == cudaSuccess &&
              cudaMemset(h->abort_word, 0, sizeof(unsigned)) == cudaSuccess &&

@@ -36,6 +36,10 @@ inline int current_device_sm_count() {
     return v;
 }
 
+// Warps per CTA of the ring executor at most (512 threads): each warp has a
+// progress word of its own.
+constexpr int kRingMaxWarps = 16;
+
 // Rank pointers travel in the kernel parameters for p <= kInlineP; larger p
 // read a device-side table kept in the handle's scratch.
 constexpr int kInlineP = 64;
@@ -125,7 +129,8 @@ struct RingArgs {
     unsigned *epoch_word;
     unsigned *finish_count;
     int flag_capacity;                // progress words to clear when the epoch wraps
-    unsigned long long *flags;        // [p * channels] progress words
+    unsigned long long *flags;        // progress words: [p * channels * warps per CTA] for the
+                                      // ring executor, [p * channels] for the tree executor
     // The low-latency mailbox (ll.cu): words tagged with the
     // launch's epoch, so any launch that wraps the epoch clears all of them;
     // slot_words = words per (rank, step) slot.  NULL / 0 where unused.

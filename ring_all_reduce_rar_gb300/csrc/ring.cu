@@ -20,21 +20,32 @@
 // ("Multiple rings, or channels").  A channel takes its slice positions in
 // blocks of `block` and runs each block through every step before the next
 // (one position at a time by default), so the right neighbour rereads a
-// fresh partial while it is still in L2.  A CTA publishes its progress
-// after each slice with a release store of a 64-bit word
-//     (epoch << 32) | (items done in this order),
-// and the right neighbour's CTA of the same channel acquires it before it
-// reads that slice at the next step.  The epoch comes from device memory
-// (flag_sync.cuh), so the words need no reset between launches and a launch
-// captured in a CUDA graph can be replayed.
+// fresh partial while it is still in L2.
 //
-// In-place safety, per slice of a chunk and so in any processing order:
-// rank r - 1 overwrites the slice r read at reduce-scatter step s only at its
-// all-gather step s, and that write waits on a chain of flags that starts
-// with r's own release after the read (the chunk's remaining reduce-scatter
-// hops, its owner, the all-gather hops up to r - 1).  The same chain orders
-// that write after r's discard of the slice's lines, which r issues before
-// its release (PTX treats a discard as a write of an indeterminate value).
+// Hand-off per warp.  Thread t of a CTA always takes the same vectors and
+// elements of a slice (vector v of [vlo, vhi) goes to thread (v - vlo) mod
+// blockDim.x, element k of the unaligned ends to thread k mod blockDim.x),
+// and every rank cuts a chunk into the same slices, so warp w of the
+// receiving CTA reads exactly the part of a slice that warp w of the
+// sending CTA wrote at the step before.  Each warp therefore runs its own
+// chain: after its part of a slice it publishes its progress with a release
+// store of its own 64-bit word
+//     (epoch << 32) | (items done in this order),
+// and warp w of the right neighbour's CTA of the same channel acquires that
+// word before it reads its part at the next step.  No CTA barrier sits
+// between slices: a warp that finished its part moves on while the others
+// still stream, which keeps the memory pipeline full.  The epoch comes from
+// device memory (flag_sync.cuh), so the words need no reset between
+// launches and a launch captured in a CUDA graph can be replayed.
+//
+// In-place safety, per warp's part of a slice of a chunk and so in any
+// processing order: rank r - 1 overwrites the part r read at reduce-scatter
+// step s only at its all-gather step s, and that write waits on a chain of
+// progress words of the same warp index that starts with r's own release
+// after the read (the chunk's remaining reduce-scatter hops, its owner, the
+// all-gather hops up to r - 1).  The same chain orders that write after r's
+// discard of the part's lines, which r issues before its release (PTX
+// treats a discard as a write of an indeterminate value).
 //
 // Bidirectional variant ("Bidirectional rings"): channels
 // [fwd_channels, channels) run the mirrored ring (send to r - 1) on the
@@ -56,13 +67,24 @@ namespace rar {
 constexpr int kRingThreads = 512;
 constexpr int kRingUnroll = 4;
 
+// Store of a reduce-scatter partial with the L2 evict-last policy: its reader
+// (the right neighbour, one slice step later) should find it in L2, and it
+// is dropped there once read, so it never needs to reach DRAM.
+__device__ __forceinline__ void st_keep(uint4 *addr, uint4 v) {
+    asm volatile("{\n\t.reg .b64 pol;\n\tcreatepolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+                 "st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, pol;\n\t}" ::"l"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // One slice [lo, hi) of one hop: dst = reduce ? op(src, dst) : src, then the
 // owner's avg scaling if `scale`; 16-byte vectors where the slice is aligned
-// (VEC), single elements at its ends.
+// (VEC), single elements at its ends.  `partial`: the result is a
+// reduce-scatter partial that the right neighbour reads next (st_keep).
 template <int DT, int OP, bool VEC>
 __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
                                            bool scale, bool prescale_in, bool prescale_own, bool discard_src,
-                                           float inv_p) {
+                                           float inv_p, bool partial = false) {
     constexpr int hop_op = HopOf<OP>::value;
     constexpr bool prediv = OP == OP_AVG_PREDIV;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
@@ -89,13 +111,19 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
     if (!vec_path) return;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    // Both reads are the last use of their lines in L2, so both take the
+    // evict-first policy (ld.global.cs) and leave L2 to the partials still
+    // waiting for their reader: the receiver's own element is an input read
+    // once; the incoming one is a partial (dropped below), the sender's
+    // original input, or a final value that only this rank reads (the next
+    // rank reads this rank's copy).
     for (long long v = vlo + threadIdx.x; v < vhi; v += (long long)T * kRingUnroll) {
         uint4 in[kRingUnroll], own[kRingUnroll];
 #pragma unroll
         for (int u = 0; u < kRingUnroll; u++) {
             const long long vv = v + (long long)u * T;
             if (vv < vhi) {
-                in[u] = __ldcg(s4 + vv);
+                in[u] = __ldcs(s4 + vv);
                 if (reduce) own[u] = __ldcs(d4 + vv);
             }
         }
@@ -109,7 +137,7 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
                     x = hop_vec<DT, hop_op>(x, (prediv && prescale_own) ? scale_vec<DT>(own[u], inv_p) : own[u]);
                 }
                 if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
-                d4[vv] = x;
+                if (partial) st_keep(d4 + vv, x); else d4[vv] = x;
             }
         }
     }
@@ -121,7 +149,6 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
 
 template <int DT, int OP, bool VEC>
 __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __grid_constant__ RingArgs a) {
-    __shared__ int s_stop;
     __shared__ long long s_cs[RAR_MAX_P], s_ce[RAR_MAX_P], s_nsl[RAR_MAX_P];  // per chunk of the ring
     const int p = a.p;
     const int r = blockIdx.x / a.channels;
@@ -129,6 +156,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
     const bool fwd = j < a.fwd_channels;
     const int jj = fwd ? j : j - a.fwd_channels;
     const int GG = fwd ? a.fwd_channels : a.channels - a.fwd_channels;
+    const int W = blockDim.x >> 5;  // warps per CTA: one progress word each
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // this rank's ring: its size rp, its position in it, the global rank at
     // a position, and the segment of the buffer the ring works on
     // (segments and chunks in global indices; see the clamp below)
@@ -170,8 +199,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
         (a.layout == RING_INTRA && a.first_step == 0);
     const char *src = rank_ptr(a.bufs, p, nb);
     char *dst = rank_ptr(a.bufs, p, r);
-    unsigned long long *my_flag = a.flags + blockIdx.x;
-    const unsigned long long *nb_flag = a.flags + (long long)nb * a.channels + j;
+    unsigned long long *my_flag = a.flags + (long long)blockIdx.x * W + w;
+    const unsigned long long *nb_flag = a.flags + ((long long)nb * a.channels + j) * W + w;
     const long long base = L / rp, extra = L % rp;
     unsigned long long received = 0;
     const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
@@ -241,18 +270,19 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
             }
             const bool rs = step < rp - 1;
             const int s = rs ? step : step - (rp - 1);
-            if (threadIdx.x == 0) {
-                bool ok;
+            // this warp's part of the slice is ready once the same warp of
+            // the left neighbour passed this slice at the step before
+            int ok = 1;
+            if (lane == 0) {
                 if (t > 0)
                     ok = ring_wait(a, epoch, nb_flag, ((unsigned long long)epoch << 32) | (item - K + 1), r, step, sl,
                                    nb);
                 else
                     ok = ld_relaxed_u32(a.abort_word) != epoch;
                 if (ok && slow) ring_delay(a.fault_delay_ns);
-                s_stop = ok ? 0 : 1;
             }
-            __syncthreads();
-            if (s_stop) goto done;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            __syncwarp();  // orders lane 0's acquire before the other lanes' reads
             {
                 const long long ce = s_ce[c];
                 const long long lo = s_cs[c] + sl * a.slice;
@@ -260,17 +290,16 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
                 // scale: this rank becomes the chunk's owner
                 ring_slice<DT, OP, VEC>(src, dst, lo, hi, rs, scale_here && rs && s == rp - 2,
                                         prediv_here && rs && s == 0, prediv_here, discard_partials && rs && s > 0,
-                                        a.inv_p);
+                                        a.inv_p, discard_partials && rs && s < rp - 2);
                 received += (unsigned long long)(hi - lo);
             }
-            __syncthreads();
-            // the release store orders the CTA's slice stores (ordered
-            // before it by the barrier) ahead of the progress word
-            if (threadIdx.x == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
+            // the warp barrier orders the lanes' stores of this part before
+            // lane 0's release store of the progress word
+            __syncwarp();
+            if (lane == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
         }
     }
-done:
-    if (threadIdx.x == 0) a.recv_counts[blockIdx.x] = received;
+    if (threadIdx.x == 0) a.recv_counts[blockIdx.x] = received;  // (warp 0 takes part in every slice)
     launch_epoch_end(a, epoch);
 }
 

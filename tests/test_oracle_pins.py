@@ -552,12 +552,18 @@ def test_tree_order_fp32_error_bound():
         assert np.all(np.abs(bufs[0] - ref) <= 4 * p * 2.0 ** -24 * mag)
 
 
-def test_tree_sampled_equals_full():
-    p, n = 7, 50
-    bufs = _rand_bufs(p, n, "float32", 99)
-    folded = oracle.fold_sampled(np.stack(bufs), np.arange(n), n, "float32", "sum", "tree")
-    oracle.tree_fold(bufs, "float32", "sum")
-    np.testing.assert_array_equal(bufs[3], folded)
+@pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "sum"), ("float32", "max"),
+                                      ("bfloat16", "avg"), ("int32", "sum")])
+def test_tree_sampled_equals_full(dtype, op):
+    """The per-element tree fold (used for the full-size checks of the tree
+    executor) equals the whole-buffer tree fold on every rank, for odd, even
+    and large p."""
+    for p, n in [(2, 33), (7, 50), (8, 257), (64, 130)]:
+        bufs = _rand_bufs(p, n, dtype, 99 + p)
+        folded = oracle.fold_sampled(np.stack(bufs), np.arange(n), n, dtype, op, "tree")
+        oracle.tree_fold(bufs, dtype, op)
+        for b in bufs:
+            np.testing.assert_array_equal(b, folded)
 
 
 # ------------------------------------------------------------- trivial cases

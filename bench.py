@@ -52,6 +52,43 @@ def roofline_bytes(engine: str, p: int, n: int, e: int) -> int:
     return 5 * (p - 1) * n * e
 
 
+def dram_floor_bytes(p: int, n: int, e: int) -> int:
+    """DRAM bytes no in-place all-reduce can go below: every rank's input
+    read once and its result written once, whatever the engine."""
+    return 2 * p * n * e
+
+
+def roofline_object(engine: str, p: int, n: int, e: int, ms_per_launch: float, peak: float, peak_kind: str,
+                    traffic):
+    """The bench line's roofline object for one engine.
+
+    frac: the engine's algorithmic bytes (roofline_bytes) per launch time
+    over the HBM peak.  For the fused engine these are the DRAM floor, so
+    frac is a true fraction of HBM bandwidth.  For the executors they count
+    the schedule's element moves, 5 (p - 1) n e, most of which L2 serves:
+    that frac is not bounded by HBM peak.  dram_frac (measured DRAM bytes,
+    `traffic`) and floor_frac (the 2 p n e floor) are the bounded ones."""
+    R = roofline_bytes(engine, p, n, e)
+    F = dram_floor_bytes(p, n, e)
+    sec = ms_per_launch * 1e-3
+    achieved = R / sec / 1e9
+    obj = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+           "frac": round(achieved / peak, 4), "traffic": traffic, "algorithmic_bytes": R,
+           "peak_kind": f"of {peak_kind}",
+           "frac_kind": ("DRAM floor bytes (inputs read once, results written once) per launch time"
+                         if R == F else
+                         "algorithmic element moves 5(p-1)Ne per launch time; L2 serves part of them, "
+                         "so this is not bounded by HBM peak (see dram_frac, floor_frac)"),
+           "floor_bytes": F, "floor_frac": round(F / sec / 1e9 / peak, 4)}
+    if traffic:
+        obj["dram_frac"] = round(traffic / sec / 1e9 / peak, 4)
+        obj["l2_served"] = round(1.0 - traffic / R, 4)
+    else:
+        obj["dram_frac"] = None
+        obj["l2_served"] = None
+    return obj
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -214,6 +251,36 @@ def time_e2e(rar, engine, host_rows, op, steps, warmup, dist_ctx):
     return dist_ctx.max(ms)
 
 
+def host_link_copy_gbs(dev_buf, nbytes: int = 1 << 30, reps: int = 3):
+    """Copy rate of the host link with both directions busy: a pinned-host to
+    device copy and a device to pinned-host copy of `nbytes` each, on two
+    streams at once (bytes both ways over the time), best of `reps`.  The
+    yardstick for the host-buffer call, which reads its inputs from and
+    writes its results to host memory at the same time."""
+    try:
+        flat = dev_buf.view(-1).view(torch.uint8)
+        nbytes = min(nbytes, flat.numel() // 2)
+        h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        d_in, d_out = flat[:nbytes], flat[nbytes:2 * nbytes]
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            with torch.cuda.stream(s1):
+                d_in.copy_(h_in, non_blocking=True)
+            with torch.cuda.stream(s2):
+                h_out.copy_(d_out, non_blocking=True)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        del h_in, h_out
+        return round(2 * nbytes / best / 1e9, 1)
+    except RuntimeError:
+        return None
+
+
 class DistCtx:
     def __init__(self):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -285,15 +352,11 @@ def run_ours(args):
         for eng in engines:
             ms = time_engine(rar, eng, rows, op, args.steps, args.warmup, ctx)
             per_step = ms / args.steps
-            R = roofline_bytes(eng, p, n, e)
-            achieved = R / (per_step * 1e-3) / 1e9
             results[eng] = {
                 "value": round(ctx.world * p * n * e / (per_step * 1e-3) / 1e9, 2),
                 "ms_per_step": round(per_step, 4),
-                "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                             "unit": "GB/s", "frac": round(achieved / peak, 4),
-                             "traffic": stored_traffic(eng, args.workload),
-                             "algorithmic_bytes": R, "peak_kind": f"of {peak_kind}"},
+                "roofline": roofline_object(eng, p, n, e, per_step, peak, peak_kind,
+                                            stored_traffic(eng, args.workload)),
             }
     clocks = clk.summary()
     head = engines[0]
@@ -308,13 +371,19 @@ def run_ours(args):
         except RuntimeError as ex:
             e2e = {"value": None, "unit": "GB/s", "unavailable": f"pinned host buffers: {ex}"[:200]}
         if host_rows is not None:
-            ms = time_e2e(rar, e2e_engine, host_rows, op, max(3, args.steps // 4), 1, ctx)
-            k = max(3, args.steps // 4)
+            k = args.steps
+            ms = time_e2e(rar, e2e_engine, host_rows, op, k, args.warmup, ctx)
+            link = host_link_copy_gbs(big)
+            host_gbs = 2 * p * n * e / (ms / k * 1e-3) / 1e9
             e2e = {"value": round(ctx.world * p * n * e / (ms / k * 1e-3) / 1e9, 2), "unit": "GB/s",
                    "h2d_bytes_per_step": p * n * e, "d2h_bytes_per_step": p * n * e,
-                   "engine": e2e_engine, "steps": k, "ms_per_step": round(ms / k, 3),
+                   "engine": e2e_engine, "steps": k, "warmup": args.warmup, "ms_per_step": round(ms / k, 3),
                    "mode": "rar_allreduce_host on pinned host buffers: the kernel reads the inputs from and "
-                           "writes the results to host memory over the host link (no staging copies)"}
+                           "writes the results to host memory over the host link (no staging copies)",
+                   "bound": "host link: every step moves 2 p N e bytes across it (inputs in, results out)",
+                   "host_link_gbs": round(host_gbs, 1),
+                   "host_link_copy_gbs": link,
+                   "host_link_frac": round(host_gbs / link, 4) if link else None}
             del host_big, host_rows
     cpu = None
     if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:

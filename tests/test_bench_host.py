@@ -42,7 +42,9 @@ def test_stored_traffic_lookup():
         d = json.load(f)
     entries = d["p8_n1073741824_bf16"]
     for eng, ent in entries.items():
-        assert ent["dram_bytes_per_launch"] == 16 * ent["captured_bytes"], eng
+        # captured at the full size (scale 1) or on a smaller case scaled by
+        # the elements processed
+        assert ent["dram_bytes_per_launch"] == ent.get("scale", 16) * ent["captured_bytes"], eng
         got = bench.stored_traffic(eng, "p8_n1073741824_bf16")
         # reported only while the engine's code is the code that was captured
         if ent["kernel_source_hash"] == bench.kernel_source_hash(eng):
@@ -60,3 +62,23 @@ def test_traffic_below_algorithmic_bytes(eng):
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         ent = json.load(f)["p8_n1073741824_bf16"][eng]
     assert 0 < ent["dram_bytes_per_launch"] <= bench.roofline_bytes(eng, 8, 1 << 30, 2)
+
+
+def test_roofline_object_fractions():
+    """frac uses the engine's algorithmic bytes; for the fused engine those
+    are the DRAM floor 2 p N e (frac == floor_frac); for the executors the
+    5 (p - 1) N e element moves, beside which dram_frac (measured bytes) and
+    floor_frac are the bounded fractions."""
+    p, n, e, peak = 8, 1 << 30, 2, 6657.0
+    fused = bench.roofline_object("fused", p, n, e, 5.2, peak, "measured", 33_000_000_000)
+    assert fused["frac"] == fused["floor_frac"]
+    assert fused["floor_bytes"] == 2 * p * n * e
+    assert abs(fused["frac"] - 2 * p * n * e / 5.2e-3 / 1e9 / peak) < 1e-4
+    assert abs(fused["dram_frac"] - 33e9 / 5.2e-3 / 1e9 / peak) < 1e-4
+    ring = bench.roofline_object("ring", p, n, e, 7.7, peak, "measured", 40_000_000_000)
+    assert ring["algorithmic_bytes"] == 5 * (p - 1) * n * e
+    assert ring["frac"] > 1.0 > ring["dram_frac"] > ring["floor_frac"]
+    assert abs(ring["l2_served"] - (1 - 40e9 / (5 * (p - 1) * n * e))) < 1e-4
+    assert "not bounded" in ring["frac_kind"]
+    none = bench.roofline_object("tree", p, n, e, 11.0, peak, "fallback", None)
+    assert none["dram_frac"] is None and none["l2_served"] is None and none["peak_kind"] == "of fallback"

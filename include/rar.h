@@ -179,8 +179,8 @@ typedef struct {
 /* Bytes of the low-latency mailbox each handle allocates in rar_init. */
 #define RAR_LL_MAILBOX_BYTES (64u << 20)
 
-/* Create a handle on `device`; allocates the ring engines' flags, counters
- * and status word there (a few hundred KB) and the low-latency mailbox
+/* Create a handle on `device`; allocates the ring and tree engines' progress
+ * words, counters and status word there (about 8.5 MB) and the low-latency mailbox
  * (RAR_LL_MAILBOX_BYTES).  opt may be NULL.
  * Errors: RAR_EINVAL (out NULL, bad device or option), RAR_ENOMEM,
  * RAR_ECUDA. */

@@ -167,6 +167,7 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.split = (long long)n;
     a.slice = slice;
     a.block = 1;  // one slice position at a time through every step, as the handle's default
+    a.tree_scale = 0;
     a.first_step = 0;
     a.n_steps = 2 * (p - 1);
     a.inv_p = 1.0f / (float)p;

@@ -15,7 +15,10 @@ namespace {
 using namespace rar;
 
 constexpr int kMaxRingCtas = 8192;           // counters capacity; CTAs of a ring or tree launch
-constexpr int kFlagWords = kMaxRingCtas * kRingMaxWarps;  // progress words (one per ring warp)
+// progress words: one per warp of a ring launch, one per (rank, slice) of a
+// tree launch (8 MB)
+constexpr int kFlagWords = 1 << 20;
+static_assert(kFlagWords >= kMaxRingCtas * kRingMaxWarps, "a progress word per ring warp");
 constexpr int kRingPhases = 3;               // counter arrays: one per ring launch of a call
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 // Shortest accepted rar_options.timeout_ns: a bound on waits of a few
@@ -204,6 +207,7 @@ RingArgs handle_ring_args(const rar_ctx *h, const RankPtrs &ptrs, int p, size_t 
     a.split = n_total;
     a.slice = 0;
     a.block = 0;
+    a.tree_scale = 0;
     a.first_step = 0;
     a.n_steps = 0;
     a.inv_p = 1.0f / (float)p;
@@ -372,38 +376,54 @@ int launch_tree_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     return RAR_OK;
 }
 
-// The tree executor: every co-resident CTA, slices of about n / channels.
+// The tree executor.  CTAs: rank r gets scale * w_r of them (w_r: the steps
+// it takes part in, 2 (p - 1) in all), with the largest scale that fits the
+// co-resident grid, so that every CTA carries about the same work; when even
+// scale 1 does not fit, or `channels` is set, every rank gets the same
+// number.  Slices: up to 128 KB, with one progress word per (rank, slice).
 int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dtype, int op, bool vec16,
                          cudaStream_t stream) {
     const int threads = h->opt.block_threads ? h->opt.block_threads : 512;
     if (threads > 512) return fail(h, RAR_EINVAL, "the tree executor runs at most 512 threads per CTA");
     const int max_ctas = std::min(tree_max_coresident_ctas(dtype, op, vec16, threads), kMaxRingCtas);
-    int G = h->opt.channels ? h->opt.channels : std::max(1, max_ctas / p);
-    if ((long long)G * p > max_ctas) {
-        if (h->opt.channels) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
-        G = max_ctas / p;
-        if (G < 1) return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
+    int scale = 0, G = 0;
+    if (h->opt.channels) {
+        G = h->opt.channels;
+        if ((long long)G * p > max_ctas) return fail(h, RAR_EUNSUPPORTED, "p * channels CTAs cannot be co-resident on this GPU");
+    } else {
+        scale = max_ctas / (2 * (p - 1));
+        if (scale < 1) {
+            G = max_ctas / p;
+            if (G < 1) return fail(h, RAR_EUNSUPPORTED, "p = " + std::to_string(p) + " rank groups cannot be co-resident");
+        }
     }
-    if (!h->opt.channels) G = (int)std::min<long long>(G, std::max<long long>(1, ((long long)n + 1023) / 1024));
+    // the CTAs of the rank with the least work (odd ranks: one step)
+    const long long g_min = scale > 0 ? scale : G;
     long long slice = h->opt.slice_elems;
     if (slice == 0) {
-        slice = ((long long)n + G - 1) / G;
+        slice = ((long long)n + g_min - 1) / g_min;
         slice = std::min<long long>(std::max<long long>((slice + 1023) / 1024 * 1024, 1024),
                                     kRingMaxSliceBytes / elem_bytes(dtype));
     }
     slice = std::max<long long>(16, (slice + 15) / 16 * 16);
-    while (((long long)n + slice - 1) / slice / G > kMaxSlicesPerChannelStep - 1) slice *= 2;
+    // one progress word per (rank, slice)
+    while ((long long)p * (((long long)n + slice - 1) / slice) > kFlagWords) slice *= 2;
     cudaError_t ce = cudaMemsetAsync(h->recv_counts, 0, sizeof(unsigned long long) * (size_t)p, stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the send counters");
     RingArgs a = handle_ring_args(h, ptrs, p, n, 0, (long long)n);  // the tree's order ignores the index
     a.layout = TREE;
     a.channels = G;
     a.fwd_channels = G;
+    a.tree_scale = scale;
     a.slice = slice;
-    // slice order: two slice positions at a time through every level (p = 8,
-    // 16 GiB bf16 on GB300: 11.9 ms, against 12.2 one at a time and 13.7
-    // level by level; a reader finds the child's or parent's fresh slice in L2)
-    a.block = h->opt.slice_block ? h->opt.slice_block : 2;
+    // slice groups of the wavefront: slice_block slices per CTA of the
+    // least-loaded ranks.  Default (GB300, bf16/int32): 1 when that gives at
+    // least 128 groups, 2 below (p = 8 x 2^30 bf16: 9.07 / 9.72 ms for 1 / 2;
+    // p = 16 x 4^13 int32: 2.56 / 2.66 ms; p = 64 x 2^24 bf16, 85 groups:
+    // 1.81 / 1.55 ms; p = 8 x 6.5 M fp32, 6 groups: 166 / 154 us)
+    const long long nsl = ((long long)n + slice - 1) / slice;
+    const int block = h->opt.slice_block ? h->opt.slice_block : (nsl >= 128 * g_min ? 1 : 2);
+    a.block = (long long)block * g_min;
     ce = launch_tree(a, dtype, op, vec16, threads, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "tree grid cannot be co-resident");

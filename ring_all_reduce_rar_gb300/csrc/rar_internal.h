@@ -120,6 +120,8 @@ struct RingArgs {
     long long split;     // bidirectional: first global index of the second half (n_total otherwise)
     long long slice;     // elements per slice
     long long block;     // slice positions per block of the processing order (0: all)
+    int tree_scale;      // tree executor: rank r runs tree_scale * w_r CTAs (w_r: the
+                         // steps it takes part in); 0: `channels` CTAs per rank
     int first_step;      // global schedule steps [first_step, first_step + n_steps)
     int n_steps;
     float inv_p;
@@ -130,7 +132,7 @@ struct RingArgs {
     unsigned *finish_count;
     int flag_capacity;                // progress words to clear when the epoch wraps
     unsigned long long *flags;        // progress words: [p * channels * warps per CTA] for the
-                                      // ring executor, [p * channels] for the tree executor
+                                      // ring executor, [p * slices] for the tree executor
     // The low-latency mailbox (ll.cu): words tagged with the
     // launch's epoch, so any launch that wraps the epoch clears all of them;
     // slot_words = words per (rank, step) slot.  NULL / 0 where unused.
@@ -164,6 +166,9 @@ cudaError_t launch_fused_hier(const FusedArgs &a, int dtype, int op, int g, bool
 // send counters, zeroed by the caller before the launch.
 cudaError_t launch_tree(const RingArgs &a, int dtype, int op, bool vec16, int threads, cudaStream_t stream);
 int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads);
+// CTAs of a tree launch: tree_scale * 2 (p - 1), or p * channels when
+// tree_scale is 0.
+long long tree_grid_ctas(int p, int tree_scale, int channels);
 // Largest co-resident grid for the ring kernel of this dtype/op (per device).
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm);
 // Low-latency hand-offs (ll.cu), p * channels CTAs of ring_ll_threads()

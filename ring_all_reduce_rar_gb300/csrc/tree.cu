@@ -3,7 +3,7 @@
 // "Derive the cost of a ring all-reduce" compares the ring with a tree
 // all-reduce: a reduce up a binary tree and a broadcast down, about
 // 2 log2(n) steps instead of 2(n - 1), so fewer step latencies on small
-// buffers.  Here p rank groups of `channels` CTAs (one cooperative launch)
+// buffers.  Here groups of CTAs (one cooperative launch) play the p ranks and
 // run L = ceil(log2 p) reduce levels and L broadcast levels over the whole
 // buffer, slice-pipelined like the ring executor:
 //   reduce level l:    rank r with r mod 2^(l+1) == 0 and r + 2^l < p
@@ -17,15 +17,79 @@
 // Element moves: (p - 1) reduce hops of 3 moves and (p - 1) broadcast hops of
 // 2, the same 5 (p - 1) n as the ring.
 //
-// Hand-offs use the progress words of flag_sync.cuh, counting items (slice
-// block, step, slice) in processing order; a rank with nothing to do at a
-// step still passes its items so that waiters move on.  Every wait is
-// bounded.
+// Work per rank.  Rank r takes part in w_r of the 2L steps: the root in its L
+// reduce levels; any other rank in the reduce levels l < ctz(r) where it has
+// a child (r + 2^l < p) and in one broadcast level, ctz(r).  The w_r add up
+// to 2 (p - 1), but they range from 1 (odd ranks) to L, so equal CTA groups
+// would leave most CTAs idle at every step.  Rank r gets tree_scale * w_r
+// CTAs instead (or `channels` CTAs each when 2 (p - 1) CTAs do not fit), so
+// every CTA carries about the same work: CTA j of rank r takes slices j,
+// j + G_r, ... and runs only the rank's active steps.
+//
+// Hand-offs: one progress word per (rank, slice), holding
+// (epoch << 32) | (active steps the rank has completed on that slice).  A
+// parent at reduce level l needs its child c's subtree partial, complete
+// once c has done all its reduce levels (w_c - 1 steps); a child at its
+// broadcast level needs its parent's final value, complete once the parent
+// has done all its w_P steps.  Both conditions also order every overwrite
+// after the reads of the old value: a rank's buffer is overwritten by its
+// broadcast only after its parent finished, which includes reading it.
+// Every wait is bounded.
+//
+// L2 policies: a reduce level reads the child's data and its own for the
+// last time (the child's partial is dropped from L2 once read, its own is
+// overwritten), so both reads take the evict-first policy, and a partial
+// that the next level reads is stored with the evict-last policy.  A
+// broadcast level l >= 1 reads a parent that its other children read again
+// at lower levels, so those reads keep the normal policy; level 0 is the
+// last read.
 #include "flag_sync.cuh"
 
 namespace rar {
 
 constexpr int kTreeThreads = 512;
+
+// ceil(log2 p)
+__host__ __device__ inline int tree_levels(int p) {
+    int L = 0;
+    while ((1 << L) < p) L++;
+    return L;
+}
+// Reduce levels in which rank r is a parent: l < ctz(r) (all L for the
+// root) with r + 2^l < p; they are 0 .. m - 1.
+__host__ __device__ inline int tree_reduce_levels(int r, int p, int L) {
+    int m = 0;
+    while (m < L && (r == 0 || ((r >> m) & 1) == 0) && r + (1 << m) < p) m++;
+    return m;
+}
+// w_r: the steps rank r takes part in (its reduce levels, plus one
+// broadcast for every rank but the root).
+__host__ __device__ inline int tree_weight(int r, int p, int L) {
+    return tree_reduce_levels(r, p, L) + (r == 0 ? 0 : 1);
+}
+// First CTA of rank r: scale * (w_0 + ... + w_(r-1)), or r * channels when
+// scale is 0.  The sum in closed form: the root's L, one broadcast for each
+// of ranks 1 .. r - 1, and per level l the ranks q in [1, r - 1] with
+// 2^(l+1) | q and q + 2^l < p.
+__host__ __device__ inline long long tree_first_cta(int r, int p, int L, int scale, int channels) {
+    if (scale <= 0) return (long long)r * channels;
+    if (r == 0) return 0;
+    long long s = L + (r - 1);
+    for (int l = 0; l < L; l++) {
+        const long long M = (long long)(r - 1 < p - (1 << l) - 1 ? r - 1 : p - (1 << l) - 1);
+        if (M >= 1) s += M >> (l + 1);
+    }
+    return s * scale;
+}
+
+
+// Store with the L2 evict-last policy (a partial that the next level reads).
+__device__ __forceinline__ void tree_st_keep(uint4 *addr, uint4 v) {
+    asm volatile("{\n\t.reg .b64 pol;\n\tcreatepolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+                 "st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, pol;\n\t}" ::"l"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 
 // One slice [lo, hi): reduce: dst = op(dst, src) (+ the root's avg scaling);
 // broadcast: dst = src.  discard_src: src is a child's partial that nobody
@@ -33,7 +97,7 @@ constexpr int kTreeThreads = 512;
 // from L2 once read, so that it is not written back.
 template <int DT, int OP, bool VEC>
 __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long lo, long long hi, bool reduce,
-                                           bool scale, bool discard_src, float inv_p) {
+                                           bool scale, bool discard_src, bool last_read, bool keep, float inv_p) {
     constexpr int hop_op = HopOf<OP>::value;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
     const int T = blockDim.x;
@@ -56,10 +120,10 @@ __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long
         const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
         for (long long v = vlo + threadIdx.x; v < vhi; v += T) {
-            uint4 x = __ldcg(s4 + v);
+            uint4 x = last_read ? __ldcs(s4 + v) : __ldcg(s4 + v);
             if (reduce) x = hop_vec<DT, hop_op>(__ldcs(d4 + v), x);
             if (OP == OP_AVG && scale) x = scale_vec<DT>(x, inv_p);
-            d4[v] = x;
+            if (keep) tree_st_keep(d4 + v, x); else d4[v] = x;
         }
         if (discard_src) discard_read_lines(s4, vlo, vhi, T);
     }
@@ -67,70 +131,65 @@ __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long
 
 template <int DT, int OP, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __grid_constant__ RingArgs a) {
-    __shared__ int s_stop;
+    __shared__ int s_stop, s_rank, s_j, s_g;
     const int p = a.p;
-    const int r = blockIdx.x / a.channels;
-    const int j = blockIdx.x % a.channels;
-    int L = 0;
-    while ((1 << L) < p) L++;
+    const int L = tree_levels(p);
+    if (threadIdx.x == 0) {
+        // this CTA's rank: the last r whose first CTA is at or before it
+        int lo = 0, hi = p - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (tree_first_cta(mid, p, L, a.tree_scale, a.channels) <= (long long)blockIdx.x) lo = mid;
+            else hi = mid - 1;
+        }
+        s_rank = lo;
+        s_j = (int)(blockIdx.x - tree_first_cta(lo, p, L, a.tree_scale, a.channels));
+        s_g = a.tree_scale > 0 ? a.tree_scale * tree_weight(lo, p, L) : a.channels;
+    }
+    __syncthreads();
+    const int r = s_rank, j = s_j, G = s_g;
     char *mine = rank_ptr(a.bufs, p, r);
-    unsigned long long *my_flag = a.flags + blockIdx.x;
     const long long nsl = (a.n + a.slice - 1) / a.slice;
+    unsigned long long *my_flags = a.flags + (long long)r * nsl;  // one per slice
     const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
     const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
-    // Processing order, as in the ring executor: this channel's slice
-    // positions (loc = 0, 1, ...) in blocks of K, each block through every
-    // step before the next, so that a reader finds the slice it waited for
-    // still in L2; progress words count the items (block, step, k) in this
-    // order, and a rank with nothing to do at a step still passes its items.
-    const int max_locs = nsl > j ? (int)((nsl - j + a.channels - 1) / a.channels) : 0;
-    const int K = a.block > 0 && a.block < max_locs ? (int)a.block : (max_locs > 0 ? max_locs : 1);
-    const int S = 2 * L;
-    const unsigned n_items = (unsigned)((max_locs + K - 1) / K) * (unsigned)S * (unsigned)K;
+    // the rank's active steps: reduce levels 0 .. m - 1, then (not the root)
+    // the broadcast at level b = ctz(r)
+    const int b = r == 0 ? L : __ffs(r) - 1;
+    const int m = tree_reduce_levels(r, p, L);
+    const int S = m + (r == 0 ? 0 : 1);
+    // Processing order: a wavefront over global slice groups [g B, (g + 1) B)
+    // (B = a.block).  At time tau a CTA runs each of the rank's active steps,
+    // of schedule step lambda, on its slices of group tau - lambda.  Every
+    // wait is for an earlier schedule step on the same group, which its
+    // owner runs at an earlier time, so the CTA at the earliest time is never
+    // blocked and the launch cannot deadlock, whatever the CTA counts; and
+    // a reader usually finds the data produced one time step before, still
+    // in L2, while every rank keeps several groups in flight.
+    const long long B = a.block > 0 ? a.block : 1;
+    const long long ngroups = (nsl + B - 1) / B;
     const unsigned epoch = launch_epoch_begin(a);
     if (muted) goto done;
 
-    {
-        int k = 0, t = 0, loc0 = 0;  // item's k and step, first slice position of its block
-        for (unsigned item = 0; item < n_items; item++) {
-            if (item > 0 && ++k == K) {  // next (block, step)
-                k = 0;
-                if (++t == S) {
-                    t = 0;
-                    loc0 += K;
-                }
-            }
-            const long long sl = j + (long long)(loc0 + k) * a.channels;
-            if (sl >= nsl) {  // past the last slice: the rest of this (block, step) is empty too
-                item += (unsigned)(K - 1 - k);
-                k = K - 1;
-                continue;
-            }
-            const bool up = t < L;
-            const int l = up ? t : 2 * L - 1 - t;
-            const int span = 1 << l;
-            int peer = -1;  // the rank read at this step
-            if (up) {
-                if ((r & (2 * span - 1)) == 0 && r + span < p) peer = r + span;
-            } else {
-                if ((r & (2 * span - 1)) == span) peer = r - span;
-            }
-            if (peer < 0) {
-                // nothing to do at this step: pass the whole (block, step) at once
-                item += (unsigned)(K - 1 - k);
-                k = K - 1;
-                if (threadIdx.x == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
-                continue;
-            }
-            {
-                const char *src = rank_ptr(a.bufs, p, peer);
-                const unsigned long long *peer_flag = a.flags + (long long)peer * a.channels + j;
+    for (long long tau = 0; tau < ngroups + 2 * L; tau++) {
+        for (int t = S - 1; t >= 0; t--) {  // the oldest group first
+            const bool up = t < m;
+            const int l = up ? t : b;
+            const int step = up ? l : 2 * L - 1 - l;  // lambda
+            const long long g = tau - step;
+            if (g < 0 || g >= ngroups) continue;
+            const long long g0 = g * B, g1 = g0 + B < nsl ? g0 + B : nsl;
+            const long long s_first = g0 + (((long long)j - g0 % G) % G + G) % G;  // first s >= g0, s = j (mod G)
+            const int peer = up ? r + (1 << l) : r - (1 << l);
+            // the peer's active steps that must be complete on the slice
+            const int need = up ? tree_weight(peer, p, L) - 1 : tree_weight(peer, p, L);
+            const char *src = rank_ptr(a.bufs, p, peer);
+            for (long long sl = s_first; sl < g1; sl += G) {
                 if (threadIdx.x == 0) {
-                    // the peer's data is final for this slice once it passed
-                    // the same slice at step t - 1 (K items earlier)
-                    bool ok = t > 0 ? ring_wait(a, epoch, peer_flag, ((unsigned long long)epoch << 32) | (item - K + 1),
-                                                r, t, sl, peer)
-                                    : ld_relaxed_u32(a.abort_word) != epoch;
+                    bool ok = need > 0 ? ring_wait(a, epoch, a.flags + (long long)peer * nsl + sl,
+                                                   ((unsigned long long)epoch << 32) | (unsigned)need, r, step, sl,
+                                                   peer)
+                                       : ld_relaxed_u32(a.abort_word) != epoch;
                     if (ok && slow) ring_delay(a.fault_delay_ns);
                     s_stop = ok ? 0 : 1;
                 }
@@ -138,14 +197,19 @@ __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __
                 if (s_stop) goto done;
                 const long long lo = sl * a.slice;
                 const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
-                // from level 1 up the child holds a partial sum of its subtree
-                tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, up && r == 0 && l == L - 1, up && l > 0, a.inv_p);
+                // from level 1 up the child holds a partial of its subtree;
+                // below the root's last level the result is a partial
+                const bool root_last = r == 0 && l == L - 1;
+                tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, up && root_last, up && l > 0, up || l == 0,
+                                        up && !root_last, a.inv_p);
                 __syncthreads();
-                if (threadIdx.x == 0) atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // the peer sent
+                if (threadIdx.x == 0) {
+                    atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // the peer sent
+                    // the release store orders the CTA's slice stores
+                    // (ordered before it by the barrier) ahead of the word
+                    st_release_u64(my_flags + sl, ((unsigned long long)epoch << 32) | (unsigned)(t + 1));
+                }
             }
-            // the release store orders the CTA's slice stores (ordered before
-            // it by the barrier) ahead of the progress word
-            if (threadIdx.x == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
         }
     }
 done:
@@ -156,7 +220,8 @@ template <int DT, int OP, bool VEC>
 static cudaError_t launch_tree_t(const RingArgs &a, int threads, cudaStream_t stream) {
     void *args[] = {const_cast<RingArgs *>(&a)};
     return cudaLaunchCooperativeKernel((const void *)tree_executor_kernel<DT, OP, VEC>,
-                                       dim3((unsigned)(a.p * a.channels)), dim3((unsigned)threads), args, 0, stream);
+                                       dim3((unsigned)tree_grid_ctas(a.p, a.tree_scale, a.channels)),
+                                       dim3((unsigned)threads), args, 0, stream);
 }
 
 template <int DT, int OP>
@@ -181,6 +246,10 @@ template <int DT, int OP>
 static int tree_occ(bool vec16, int threads) {
     return vec16 ? tree_occ_of(tree_executor_kernel<DT, OP, true>, threads)
                  : tree_occ_of(tree_executor_kernel<DT, OP, false>, threads);
+}
+
+long long tree_grid_ctas(int p, int tree_scale, int channels) {
+    return tree_first_cta(p, p, tree_levels(p), tree_scale, channels) + 0;
 }
 
 int tree_max_coresident_ctas(int dtype, int op, bool vec16, int threads) {

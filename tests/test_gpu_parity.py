@@ -402,6 +402,24 @@ def test_slice_order_does_not_change_results(rar, dev, engine, extra):
             assert got == list(sends)
 
 
+def test_tree_weighted_ctas_any_group_size(rar, dev):
+    """The tree executor's default grid gives rank r a CTA count in proportion
+    to the steps it takes part in, and walks slice groups as a wavefront.
+    Any slice size and group size, odd and even p, gives the tree order's
+    bits and sends n up plus n per child."""
+    for p, n in [(3, 3 * 7000 + 1), (8, 8 * 30000 + 13), (13, 13 * 5000 + 6), (64, 64 * 600 + 3)]:
+        host = gen(p, n, "bfloat16", ("normal", 1e-2), 40 + p)
+        ref, _ = oracle_expect(host, "bfloat16", "sum", "tree")
+        for sl, blk in [(16, 1), (1024, 1), (1024, 2), (1024, 5), (4096, 3), (0, 0)]:
+            _, rows = upload(host, dev)
+            with rar.Handle(0, **handle_opts("tree", slice_elems=sl, slice_block=blk)) as h:
+                h.allreduce(rows)
+                h.check()
+                got = h.send_counts(p)
+            assert_bits_equal(rows, ref, f"tree p={p} slice={sl} block={blk}")
+            assert got == [(n if r else 0) + n * len(_tree_children(r, p)) for r in range(p)]
+
+
 def test_ring_back_to_back_calls_reuse_flags(rar, dev):
     host = gen(4, 4099, "float32", ("uniform", -1.0, 1.0), 3)
     ref, _ = oracle_expect(host, "float32", "sum", "ring")

@@ -59,7 +59,7 @@ def dram_floor_bytes(p: int, n: int, e: int) -> int:
 
 
 def roofline_object(engine: str, p: int, n: int, e: int, ms_per_launch: float, peak: float, peak_kind: str,
-                    traffic):
+                    traffic, l2_bytes=None):
     """The bench line's roofline object for one engine.
 
     frac: the engine's algorithmic bytes (roofline_bytes) per launch time
@@ -83,9 +83,16 @@ def roofline_object(engine: str, p: int, n: int, e: int, ms_per_launch: float, p
     if traffic:
         obj["dram_frac"] = round(traffic / sec / 1e9 / peak, 4)
         obj["l2_served"] = round(1.0 - traffic / R, 4)
+        obj["traffic_over_floor"] = round(traffic / F, 4)
     else:
         obj["dram_frac"] = None
         obj["l2_served"] = None
+        obj["traffic_over_floor"] = None
+    if l2_bytes:
+        # bytes through L2 (lts__t_bytes) per launch time: beside ncu's own
+        # L2 throughput percentage, the load the schedule puts on L2
+        obj["l2_bytes"] = l2_bytes
+        obj["l2_gbs"] = round(l2_bytes / sec / 1e9, 1)
     return obj
 
 
@@ -128,9 +135,10 @@ def kernel_source_hash(engine: str) -> str:
     return h.hexdigest()[:16]
 
 
-def stored_traffic(engine: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, or None if the
-    kernel changed since the capture."""
+def stored_counters(engine: str, workload: str):
+    """The committed ncu counters of one engine's launch on a workload
+    (profiles/traffic.json), or None if the kernel changed since the
+    capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -140,7 +148,14 @@ def stored_traffic(engine: str, workload: str):
     ent = d.get(workload, {}).get(engine)
     if not ent or engine not in ENGINE_SOURCES or ent.get("kernel_source_hash") != kernel_source_hash(engine):
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent
+
+
+def stored_traffic(engine: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel changed since the capture."""
+    ent = stored_counters(engine, workload)
+    return ent.get("dram_bytes_per_launch") if ent else None
 
 
 class ClockSampler:
@@ -356,7 +371,8 @@ def run_ours(args):
                 "value": round(ctx.world * p * n * e / (per_step * 1e-3) / 1e9, 2),
                 "ms_per_step": round(per_step, 4),
                 "roofline": roofline_object(eng, p, n, e, per_step, peak, peak_kind,
-                                            stored_traffic(eng, args.workload)),
+                                            stored_traffic(eng, args.workload),
+                                            (stored_counters(eng, args.workload) or {}).get("lts_bytes_per_launch")),
             }
     clocks = clk.summary()
     head = engines[0]

@@ -13,6 +13,7 @@
 #include <stdint.h>
 
 #include <type_traits>
+#include <utility>
 
 #include "rar_internal.h"
 
@@ -174,6 +175,34 @@ template <int DT>
 __device__ __forceinline__ void store_elem(char *base, long long i, uint32_t w) {
     if constexpr (ElemInfo<DT>::bytes == 4) reinterpret_cast<unsigned int *>(base)[i] = w;
     else reinterpret_cast<unsigned short *>(base)[i] = (unsigned short)w;
+}
+
+// Programmatic dependent launch.  A fused kernel is launched with
+// programmatic stream serialization, so it may be scheduled while the
+// previous kernel of the stream finishes; pdl_wait() then blocks until that
+// kernel has completed and its memory is visible (a no-op when the previous
+// operation was not a kernel), and must come before any access to the rank
+// buffers.  pdl_launch_dependents() lets the next such kernel be scheduled
+// once every CTA of this grid has run it; all of this grid's CTAs are then
+// resident, so the waiting CTAs of the next grid cannot hold them back.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kernel` with programmatic stream serialization (see pdl_wait).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ char *rank_ptr(const RankPtrs &b, int p, int r) {

@@ -18,8 +18,8 @@ static cudaError_t launch_hier_grid(K kernel, const FusedArgs &a, int g, long lo
     const long long want = (work + threads - 1) / threads;
     if (grid > want) grid = want;
     if (grid < 1) grid = 1;
-    kernel<<<(unsigned)grid, threads, 0, stream>>>(a, g);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(kernel, dim3((unsigned)grid), dim3((unsigned)threads), 0, stream, a, g);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int DT, int OP, int P>

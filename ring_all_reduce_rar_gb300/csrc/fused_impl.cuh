@@ -131,6 +131,8 @@ __device__ __forceinline__ void fused_fold_element(const FusedArgs &a, int p, in
 
 template <int DT, int OP, int P, int U, bool VEC>
 __global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const __grid_constant__ FusedArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int p = P > 0 ? P : a.p;
     const long long n = a.n;
     const long long base = a.n_total / p, extra = a.n_total % p;
@@ -235,6 +237,8 @@ __device__ __forceinline__ uint32_t tree_fold_element(const FusedArgs &a, int p,
 
 template <int DT, int OP, int P, bool VEC>
 __global__ void __launch_bounds__(kFusedThreads) fused_tree_order_kernel(const __grid_constant__ FusedArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int p = P > 0 ? P : a.p;
     const long long n = a.n;
     const long long base = a.n_total / p, extra = a.n_total % p;
@@ -350,6 +354,8 @@ __device__ __forceinline__ uint32_t hier_fold_element(const FusedArgs &a, int p,
 
 template <int DT, int OP, bool VEC>
 __global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel(const __grid_constant__ FusedArgs a, int g) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int p = a.p;
     const int m = p / g;
     const long long n = a.n;
@@ -384,6 +390,8 @@ __global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel(const __grid_
 // and P stores.  Vectors across a segment boundary fold element by element.
 template <int DT, int OP, int P, bool VEC>
 __global__ void __launch_bounds__(kFusedThreads) fused_hier_kernel_p(const __grid_constant__ FusedArgs a, int g) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int hop = HopOf<OP>::value;
     constexpr int VE = VEC ? 16 / ElemInfo<DT>::bytes : 1;
     const int m = P / g;
@@ -475,8 +483,8 @@ static cudaError_t launch_persistent(K kernel, const FusedArgs &a, long long wor
     long long grid = (long long)sms * blocks_per_sm_of(kernel, threads);
     if (grid > want) grid = want;
     if (grid < 1) grid = 1;
-    kernel<<<(unsigned)grid, threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(kernel, dim3((unsigned)grid), dim3((unsigned)threads), 0, stream, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int DT, int OP, int P>
@@ -489,9 +497,17 @@ static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int
                                      stream);
         return launch_persistent(fused_tree_order_kernel<DT, OP, P, false>, a, a.n, threads, stream);
     }
-    if (vec16)
-        return launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, a, ((a.n + VE - 1) / VE + U - 1) / U,
-                                 threads, stream);
+    if (vec16) {
+        // a buffer that one vector per thread covers within one wave of
+        // CTAs: one vector per thread, all in flight at once, instead of U
+        // per thread one after the other (at most a few tiles, each of which
+        // may cross chunk boundaries)
+        const long long nvec = (a.n + VE - 1) / VE;
+        if (U > 1 && nvec <= (long long)sm_count_cached() * threads)
+            return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, true>, a, nvec, threads, stream);
+        return launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, a, (nvec + U - 1) / U, threads,
+                                 stream);
+    }
     return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, false>, a, a.n, threads, stream);
 }
 

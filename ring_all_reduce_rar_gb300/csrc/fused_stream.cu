@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     uint64_t *empty = full + kStreamMaxStages;
     const long long my_tiles = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; s++) {
@@ -395,8 +397,8 @@ static cudaError_t launch_stream_v(const FusedArgs &a, int tile_bytes, int n_sta
     long long grid = (long long)sms * per_sm;
     if (grid > ntiles) grid = ntiles;
     if (grid < 1) grid = 1;
-    kernel<<<(unsigned)grid, kStreamThreads, smem, stream>>>(a, tile_bytes, n_stages);
-    return cudaGetLastError();
+    e = launch_pdl(kernel, dim3((unsigned)grid), dim3(kStreamThreads), smem, stream, a, tile_bytes, n_stages);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // 8 vectors per consumer thread: tiles of up to 32 KB per rank.

@@ -82,3 +82,14 @@ def test_roofline_object_fractions():
     assert "not bounded" in ring["frac_kind"]
     none = bench.roofline_object("tree", p, n, e, 11.0, peak, "fallback", None)
     assert none["dram_frac"] is None and none["l2_served"] is None and none["peak_kind"] == "of fallback"
+
+
+def test_stored_counters_carry_l2_bytes_and_reach_the_roofline():
+    ent = bench.stored_counters("ring", "p8_n1073741824_bf16")
+    if ent is None:
+        pytest.skip("the ring's code changed since its counters were captured")
+    assert ent["dram_bytes_per_launch"] == ent["dram_read_bytes"] + ent["dram_write_bytes"]
+    obj = bench.roofline_object("ring", 8, 1 << 30, 2, 7.2, 6657.0, "measured", ent["dram_bytes_per_launch"],
+                                ent["lts_bytes_per_launch"])
+    assert obj["l2_bytes"] == ent["lts_bytes_per_launch"]
+    assert obj["traffic_over_floor"] >= 1.0

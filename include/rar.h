@@ -167,14 +167,24 @@ typedef struct {
                                       ring, while p * 2 (p - 1) chunk-sized slots fit in
                                       RAR_LL_MAILBOX_BYTES; tree: while
                                       p * (ceil(log2 p) + 1) buffer-sized slots fit */
-    int slice_block;               /* ring and tree executors with progress words: each
-                                      channel takes its slices in blocks of this many and runs
-                                      a block through every step before the next, so that the
-                                      reader finds a fresh slice still in L2 (0 = auto: 1 for
-                                      the ring, 2 for the tree; a value at least the slices per
-                                      step gives the step-by-step order).  Results do not
-                                      depend on it. */
+    int slice_block;               /* ring and tree executors with progress words.  Ring:
+                                      each channel takes its slices in blocks of this many and
+                                      runs a block through every step before the next, so that
+                                      the reader finds a fresh slice still in L2 (0 = auto: 1;
+                                      a value at least the slices per step gives the
+                                      step-by-step order).  Tree: slices per CTA of the
+                                      least-loaded ranks in one group of the wavefront (0 =
+                                      auto: 1 or 2).  Results do not depend on it. */
+    int trace;                     /* nonzero: the ring executor (flat and bidirectional)
+                                      and the tree executor, with progress words, record per
+                                      rank and schedule step the time spent waiting for the
+                                      neighbour and the time spent on its slices (rar_trace).
+                                      rar_init / rar_set_options allocate the record, 2 x
+                                      RAR_MAX_P x RAR_TRACE_MAX_STEPS words (32 MB) */
 } rar_options;
+
+/* Schedule steps a trace holds per rank (2 (RAR_MAX_P - 1)). */
+#define RAR_TRACE_MAX_STEPS 2046
 
 /* Bytes of the low-latency mailbox each handle allocates in rar_init. */
 #define RAR_LL_MAILBOX_BYTES (64u << 20)
@@ -301,6 +311,24 @@ int rar_destroy(rar_handle h);
 
 /* RAR_VERSION of the loaded library. */
 int rar_version(void);
+
+/* Per-rank step times of the last call, when rar_options.trace was set and
+ * the call ran the ring executor (flat or bidirectional) or the tree
+ * executor with progress words ("Ring All-Reduce, in depth", "Failure
+ * modes": a straggler shows as the rank whose steps take longest, and its
+ * right neighbour as the one that waits longest).  For rank r and schedule
+ * step s (global step index: 0 .. 2 (p - 1) - 1 for the ring, 0 .. 2L - 1
+ * for the tree), work_ns[r * max_steps + s] is the time the rank's CTAs spent on
+ * their slices of that step (from the end of the wait to the release of the
+ * slice, summed over CTAs; an injected delay counts as work), and
+ * wait_ns[r * max_steps + s] the time they spent waiting for the neighbour's
+ * progress word; both from the first warp of each CTA, in nanoseconds of
+ * %globaltimer.  *steps receives the step count; the arrays hold
+ * p * max_steps entries.  Synchronises like rar_status.
+ * Errors: RAR_EINVAL (null argument, p differs from the last call's,
+ * max_steps too small, or the last call was not traced). */
+int rar_trace(rar_handle h, unsigned long long *work_ns, unsigned long long *wait_ns, int p, int max_steps,
+              int *steps);
 
 /* Test hook: set the handle's launch epoch counter (device memory; the next
  * ring-engine or tree launch runs with epoch + 1).  The ring engines tag

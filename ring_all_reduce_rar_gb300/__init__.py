@@ -13,7 +13,7 @@ from ._abi import (DTYPE_CODES, ENGINE_CODES, FAULT_CODES, OP_CODES, RAR_MAX_P, 
                    rar_allreduce_host, rar_allreduce_noalloc, rar_allreduce_ptrs, rar_allreduce_range, rar_debug_set_epoch,
                    rar_destroy,
                    rar_init, rar_last_error, rar_reduce_scatter, rar_send_counts, rar_set_options, rar_status,
-                   rar_version)
+                   rar_trace, rar_version)
 from ._build import build
 
 __all__ = [
@@ -22,5 +22,5 @@ __all__ = [
     "rar_allreduce_host", "rar_allreduce_noalloc", "rar_allreduce_ptrs", "rar_allreduce_range", "rar_debug_set_epoch",
     "rar_destroy",
     "rar_init", "rar_last_error", "rar_reduce_scatter", "rar_send_counts", "rar_set_options", "rar_status",
-    "rar_version",
+    "rar_trace", "rar_version",
 ]

@@ -48,12 +48,13 @@ class Options(ctypes.Structure):
         ("hier_group", ctypes.c_int),
         ("protocol", ctypes.c_int),
         ("slice_block", ctypes.c_int),
+        ("trace", ctypes.c_int),
     ]
 
 
 def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, timeout_ns=0,
                  skip_pointer_check=False, fault_mode="none", fault_rank=0, fault_delay_ns=0,
-                 fused_path="auto", hier_group=0, protocol="auto", slice_block=0) -> Options:
+                 fused_path="auto", hier_group=0, protocol="auto", slice_block=0, trace=False) -> Options:
     o = Options()
     o.engine = ENGINE_CODES[engine] if isinstance(engine, str) else int(engine)
     o.channels = channels
@@ -68,6 +69,7 @@ def make_options(engine="fused", channels=0, slice_elems=0, block_threads=0, tim
     o.hier_group = hier_group
     o.protocol = PROTOCOLS[protocol] if isinstance(protocol, str) else int(protocol)
     o.slice_block = slice_block
+    o.trace = 1 if trace else 0
     return o
 
 
@@ -106,8 +108,12 @@ def load_library():
         lib.rar_destroy.argtypes = [vp]
         lib.rar_version.argtypes = []
         lib.rar_debug_set_epoch.argtypes = [vp, ctypes.c_uint]
+        u64p = ctypes.POINTER(ctypes.c_ulonglong)
+        lib.rar_trace.argtypes = [vp, u64p, u64p, i32, i32, ctypes.POINTER(i32)]
         for name in ("rar_init", "rar_set_options", "rar_allreduce", "rar_reduce_scatter",
-                     "rar_all_gather", "rar_allreduce_range", "rar_allreduce_host", "rar_debug_set_epoch", "rar_allreduce_noalloc", "rar_status", "rar_send_counts", "rar_destroy", "rar_version"):
+                     "rar_all_gather", "rar_allreduce_range", "rar_allreduce_host", "rar_debug_set_epoch",
+                     "rar_allreduce_noalloc", "rar_status", "rar_send_counts", "rar_destroy", "rar_version",
+                     "rar_trace"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -242,6 +248,19 @@ def rar_send_counts(handle: int, p: int) -> list[int]:
     return list(out)
 
 
+def rar_trace(handle: int, p: int) -> tuple[list[list[int]], list[list[int]]]:
+    """Per-rank step times of the last traced call (see rar_trace in
+    rar.h): (work_ns, wait_ns), each p lists of one entry per schedule step."""
+    max_steps = 2046
+    work = (ctypes.c_ulonglong * (p * max_steps))()
+    wait = (ctypes.c_ulonglong * (p * max_steps))()
+    steps = ctypes.c_int()
+    _check(handle, load_library().rar_trace(handle, work, wait, p, max_steps, ctypes.byref(steps)))
+    s = steps.value
+    return ([list(work[r * max_steps:r * max_steps + s]) for r in range(p)],
+            [list(wait[r * max_steps:r * max_steps + s]) for r in range(p)])
+
+
 def rar_last_error(handle: int | None) -> str:
     return load_library().rar_last_error(handle).decode(errors="replace")
 
@@ -297,6 +316,9 @@ class Handle:
 
     def send_counts(self, p: int) -> list[int]:
         return rar_send_counts(self.h, p)
+
+    def trace(self, p: int):
+        return rar_trace(self.h, p)
 
     def close(self):
         if self.h:

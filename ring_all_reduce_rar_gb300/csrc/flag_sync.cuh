@@ -144,6 +144,17 @@ __device__ __forceinline__ void discard_read_lines(const uint4 *s4, long long vl
     }
 }
 
+// Step trace (RingArgs::trace): the first warp of a CTA adds the time it
+// waited for the neighbour and the time it then spent on the slice to its
+// rank's entry for the step.  t0: before the wait, t1: after it.
+__device__ __forceinline__ void trace_add(const RingArgs &a, int rank, int step, unsigned long long t0,
+                                          unsigned long long t1) {
+    const unsigned long long t2 = global_ns();
+    unsigned long long *e = a.trace + 2 * ((long long)rank * a.trace_steps + step);
+    atomicAdd(e, t2 - t1);      // work
+    atomicAdd(e + 1, t1 - t0);  // wait
+}
+
 // Injected straggler: pause about `ns` (bounded by the same clock).
 static __device__ void ring_delay(unsigned ns) {
     const unsigned long long t0 = global_ns();

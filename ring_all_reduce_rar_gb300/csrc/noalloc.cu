@@ -185,6 +185,8 @@ extern "C" int rar_allreduce_noalloc(void *const *bufs, int p, size_t n, int dty
     a.fault_mode = RAR_FAULT_NONE;
     a.fault_rank = 0;
     a.fault_delay_ns = 0;
+    a.trace = nullptr;
+    a.trace_steps = 0;
     ce = launch_ring(a, dtype, op, vec16, kNoAllocThreads, (cudaStream_t)stream);
     if (ce != cudaSuccess) return reject(RAR_ECUDA, std::string("launching the ring executor: ") + cudaGetErrorString(ce));
     return RAR_OK;

@@ -41,6 +41,8 @@ constexpr int kLLTreeAutoMinP = 16;
 constexpr size_t kLLTreeAutoMaxBytes = (size_t)64 << 10;
 
 thread_local std::string g_init_error;  // errors before a handle exists
+// step trace: {work, wait} per (rank, step)
+constexpr size_t kTraceWords = 2 * (size_t)RAR_MAX_P * RAR_TRACE_MAX_STEPS;
 
 }  // namespace
 
@@ -57,6 +59,9 @@ struct rar_ctx {
     unsigned *epoch_words = nullptr;  // [0] last finished launch's epoch, [1] finish counter
     void **ptr_table = nullptr;
     unsigned long long *ll_box = nullptr;  // low-latency mailbox, kLLMailboxWords
+    unsigned long long *trace = nullptr;   // step trace (rar_options.trace), kTraceWords
+    bool last_traced = false;              // the last call filled the trace
+    int last_trace_steps = 0;
     unsigned acked_seq = 0;           // status failures already reported
     // last call, for rar_status / rar_send_counts
     bool have_last = false;
@@ -225,7 +230,22 @@ RingArgs handle_ring_args(const rar_ctx *h, const RankPtrs &ptrs, int p, size_t 
     a.fault_mode = h->opt.fault_mode;
     a.fault_rank = h->opt.fault_rank;
     a.fault_delay_ns = h->opt.fault_delay_ns;
+    a.trace = nullptr;
+    a.trace_steps = 0;
     return a;
+}
+
+// Arm the step trace for a launch of `steps` schedule steps per rank: clear
+// the record (stream-ordered) and point the launch at it.
+int arm_trace(rar_ctx *h, RingArgs &a, int p, int steps, cudaStream_t stream) {
+    if (!h->opt.trace || !h->trace) return RAR_OK;
+    cudaError_t ce = cudaMemsetAsync(h->trace, 0, sizeof(unsigned long long) * 2 * (size_t)p * (size_t)steps, stream);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the step trace");
+    a.trace = h->trace;
+    a.trace_steps = steps;
+    h->last_traced = true;
+    h->last_trace_steps = steps;
+    return RAR_OK;
 }
 
 // One ring launch: `layout` picks the rings (flat; inside nodes of `group`;
@@ -295,6 +315,10 @@ int launch_ring_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, long lo
     a.first_step = first;
     a.n_steps = steps;
     a.recv_counts = h->recv_counts + (size_t)phase_idx * kMaxRingCtas;
+    if (layout == RING_FLAT) {  // (the hierarchical schedule's launches are not traced)
+        int rc = arm_trace(h, a, p, 2 * (p - 1), stream);
+        if (rc != RAR_OK) return rc;
+    }
     cudaError_t ce = launch_ring(a, dtype, op, vec16, threads, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "ring grid cannot be co-resident");
@@ -424,6 +448,10 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
     const long long nsl = ((long long)n + slice - 1) / slice;
     const int block = h->opt.slice_block ? h->opt.slice_block : (nsl >= 128 * g_min ? 1 : 2);
     a.block = (long long)block * g_min;
+    int L = 0;
+    while ((1 << L) < p) L++;
+    int rc = arm_trace(h, a, p, 2 * L, stream);
+    if (rc != RAR_OK) return rc;
     ce = launch_tree(a, dtype, op, vec16, threads, stream);
     if (ce != cudaSuccess) {
         if (ce == cudaErrorCooperativeLaunchTooLarge) return fail(h, RAR_EUNSUPPORTED, "tree grid cannot be co-resident");
@@ -449,6 +477,7 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
     h->last_ring = false;
     h->last_phases = 0;
     h->last_p = p;
+    h->last_traced = false;
     if (n == 0 || p == 1) return RAR_OK;
 
     DeviceGuard dg(h->device);
@@ -637,7 +666,8 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
               cudaMalloc((void **)&h->abort_word, sizeof(unsigned)) == cudaSuccess &&
               cudaMalloc((void **)&h->epoch_words, 2 * sizeof(unsigned)) == cudaSuccess &&
               cudaMalloc((void **)&h->ptr_table, sizeof(void *) * RAR_MAX_P) == cudaSuccess &&
-              cudaMalloc((void **)&h->ll_box, sizeof(unsigned long long) * kLLMailboxWords) == cudaSuccess;
+              cudaMalloc((void **)&h->ll_box, sizeof(unsigned long long) * kLLMailboxWords) == cudaSuccess &&
+              (!o.trace || cudaMalloc((void **)&h->trace, sizeof(unsigned long long) * kTraceWords) == cudaSuccess);
     if (ok) {
         ok = cudaMemset(h->flags, 0, sizeof(unsigned long long) * kFlagWords) == cudaSuccess &&
              cudaMemset(h->recv_counts, 0, sizeof(unsigned long long) * kMaxRingCtas * kRingPhases) == cudaSuccess &&
@@ -656,6 +686,7 @@ int rar_init(rar_handle *out, int device, const rar_options *opt) {
         cudaFree(h->epoch_words);
         cudaFree(h->ptr_table);
         cudaFree(h->ll_box);
+        cudaFree(h->trace);
         delete h;
         return fail(nullptr, RAR_ENOMEM, "allocating the handle's scratch failed");
     }
@@ -669,7 +700,41 @@ int rar_set_options(rar_handle h, const rar_options *opt) {
     if (opt) o = *opt;
     int rc = check_options(h, o);
     if (rc != RAR_OK) return rc;
+    if (o.trace && !h->trace) {
+        DeviceGuard dg(h->device);
+        if (dg.err != cudaSuccess) return cuda_fail(h, dg.err, "selecting the device");
+        if (cudaMalloc((void **)&h->trace, sizeof(unsigned long long) * kTraceWords) != cudaSuccess) {
+            cudaGetLastError();
+            h->trace = nullptr;
+            return fail(h, RAR_ENOMEM, "allocating the step trace failed");
+        }
+    }
     h->opt = o;
+    return RAR_OK;
+}
+
+int rar_trace(rar_handle h, unsigned long long *work_ns, unsigned long long *wait_ns, int p, int max_steps,
+              int *steps) {
+    if (!h) return fail(nullptr, RAR_EINVAL, "handle is NULL");
+    if (!work_ns || !wait_ns || !steps) return fail(h, RAR_EINVAL, "NULL output");
+    if (!h->have_last || p != h->last_p) return fail(h, RAR_EINVAL, "p differs from the last call's p");
+    if (!h->last_traced)
+        return fail(h, RAR_EINVAL, "the last call was not traced (rar_options.trace, ring or tree executor with "
+                                   "progress words)");
+    const int S = h->last_trace_steps;
+    *steps = S;
+    if (max_steps < S) return fail(h, RAR_EINVAL, "max_steps is below the last call's step count");
+    int rc = rar_status(h);
+    if (rc != RAR_OK && rc != RAR_ETIMEOUT) return rc;
+    DeviceGuard dg(h->device);
+    std::vector<unsigned long long> rec(2 * (size_t)p * (size_t)S);
+    cudaError_t ce = cudaMemcpy(rec.data(), h->trace, sizeof(unsigned long long) * rec.size(), cudaMemcpyDeviceToHost);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "reading the step trace");
+    for (int r = 0; r < p; r++)
+        for (int s = 0; s < S; s++) {
+            work_ns[(size_t)r * max_steps + s] = rec[2 * ((size_t)r * S + s)];
+            wait_ns[(size_t)r * max_steps + s] = rec[2 * ((size_t)r * S + s) + 1];
+        }
     return RAR_OK;
 }
 
@@ -840,6 +905,7 @@ int rar_destroy(rar_handle h) {
         cudaFree(h->epoch_words);
         cudaFree(h->ptr_table);
         cudaFree(h->ll_box);
+        cudaFree(h->trace);
     }
     delete h;
     return RAR_OK;

@@ -146,6 +146,10 @@ struct RingArgs {
     int fault_mode;
     int fault_rank;
     unsigned fault_delay_ns;
+    // per (rank, global step): {work ns, wait ns} summed over the rank's
+    // CTAs (first warp of each), trace_steps steps per rank; NULL: off
+    unsigned long long *trace;
+    int trace_steps;
 };
 
 // Launchers (return cudaError_t of the launch).  `vec16` selects the 128-bit

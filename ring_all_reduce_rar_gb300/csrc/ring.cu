@@ -147,9 +147,12 @@ __device__ __forceinline__ void ring_slice(const char *src, char *dst, long long
     if (discard_src) discard_read_lines(s4, vlo, vhi, T);
 }
 
-template <int DT, int OP, bool VEC>
+// TRACE: record the step trace (RingArgs::trace); a separate instantiation,
+// so that the untraced kernel carries none of its code.
+template <int DT, int OP, bool VEC, bool TRACE>
 __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __grid_constant__ RingArgs a) {
     __shared__ long long s_cs[RAR_MAX_P], s_ce[RAR_MAX_P], s_nsl[RAR_MAX_P];  // per chunk of the ring
+    __shared__ unsigned long long s_trace_t0, s_trace_t1;                      // (step trace)
     const int p = a.p;
     const int r = blockIdx.x / a.channels;
     const int j = blockIdx.x % a.channels;
@@ -274,11 +277,13 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
             // the left neighbour passed this slice at the step before
             int ok = 1;
             if (lane == 0) {
+                if (TRACE && w == 0) s_trace_t0 = global_ns();
                 if (t > 0)
                     ok = ring_wait(a, epoch, nb_flag, ((unsigned long long)epoch << 32) | (item - K + 1), r, step, sl,
                                    nb);
                 else
                     ok = ld_relaxed_u32(a.abort_word) != epoch;
+                if (TRACE && w == 0) s_trace_t1 = global_ns();
                 if (ok && slow) ring_delay(a.fault_delay_ns);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -296,7 +301,10 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
             // the warp barrier orders the lanes' stores of this part before
             // lane 0's release store of the progress word
             __syncwarp();
-            if (lane == 0) st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
+            if (lane == 0) {
+                st_release_u64(my_flag, ((unsigned long long)epoch << 32) | (item + 1));
+                if (TRACE && w == 0) trace_add(a, r, step, s_trace_t0, s_trace_t1);
+            }
         }
     }
     if (threadIdx.x == 0) a.recv_counts[blockIdx.x] = received;  // (warp 0 takes part in every slice)
@@ -306,8 +314,10 @@ __global__ void __launch_bounds__(kRingThreads, 2) ring_executor_kernel(const __
 template <int DT, int OP, bool VEC>
 static cudaError_t launch_ring_t(const RingArgs &a, int threads, cudaStream_t stream) {
     void *args[] = {const_cast<RingArgs *>(&a)};
-    return cudaLaunchCooperativeKernel((const void *)ring_executor_kernel<DT, OP, VEC>,
-                                       dim3((unsigned)(a.p * a.channels)), dim3((unsigned)threads), args, 0, stream);
+    const void *kernel = a.trace ? (const void *)ring_executor_kernel<DT, OP, VEC, true>
+                                 : (const void *)ring_executor_kernel<DT, OP, VEC, false>;
+    return cudaLaunchCooperativeKernel(kernel, dim3((unsigned)(a.p * a.channels)), dim3((unsigned)threads), args, 0,
+                                       stream);
 }
 
 template <int DT, int OP>
@@ -330,8 +340,9 @@ static int occ_of(K kernel, int threads) {
 
 template <int DT, int OP>
 static int ring_occ(bool vec16, int threads) {
-    return vec16 ? occ_of(ring_executor_kernel<DT, OP, true>, threads)
-                 : occ_of(ring_executor_kernel<DT, OP, false>, threads);
+    // (the traced instantiation has the same launch bounds)
+    return vec16 ? occ_of(ring_executor_kernel<DT, OP, true, false>, threads)
+                 : occ_of(ring_executor_kernel<DT, OP, false, false>, threads);
 }
 
 int ring_max_coresident_ctas(int dtype, int op, bool vec16, int threads, int *out_per_sm) {

@@ -132,6 +132,7 @@ __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long
 template <int DT, int OP, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __grid_constant__ RingArgs a) {
     __shared__ int s_stop, s_rank, s_j, s_g;
+    __shared__ unsigned long long s_trace_t0, s_trace_t1;  // (step trace)
     const int p = a.p;
     const int L = tree_levels(p);
     if (threadIdx.x == 0) {
@@ -186,10 +187,12 @@ __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __
             const char *src = rank_ptr(a.bufs, p, peer);
             for (long long sl = s_first; sl < g1; sl += G) {
                 if (threadIdx.x == 0) {
+                    if (a.trace) s_trace_t0 = global_ns();
                     bool ok = need > 0 ? ring_wait(a, epoch, a.flags + (long long)peer * nsl + sl,
                                                    ((unsigned long long)epoch << 32) | (unsigned)need, r, step, sl,
                                                    peer)
                                        : ld_relaxed_u32(a.abort_word) != epoch;
+                    if (a.trace) s_trace_t1 = global_ns();
                     if (ok && slow) ring_delay(a.fault_delay_ns);
                     s_stop = ok ? 0 : 1;
                 }
@@ -208,6 +211,7 @@ __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __
                     // the release store orders the CTA's slice stores
                     // (ordered before it by the barrier) ahead of the word
                     st_release_u64(my_flags + sl, ((unsigned long long)epoch << 32) | (unsigned)(t + 1));
+                    if (a.trace) trace_add(a, r, step, s_trace_t0, s_trace_t1);
                 }
             }
         }

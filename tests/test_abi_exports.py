@@ -31,7 +31,7 @@ def test_header_declares_the_api():
     names = declared_functions()
     for must in ("rar_init", "rar_allreduce", "rar_destroy", "rar_reduce_scatter", "rar_all_gather",
                  "rar_status", "rar_send_counts", "rar_last_error", "rar_set_options", "rar_version",
-                 "rar_allreduce_host", "rar_allreduce_range", "rar_allreduce_noalloc"):
+                 "rar_allreduce_host", "rar_allreduce_range", "rar_allreduce_noalloc", "rar_trace"):
         assert must in names
 
 
@@ -55,13 +55,13 @@ def test_options_layout_matches_c():
 #include <stddef.h>
 #include "rar.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(rar_options),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(rar_options),
     offsetof(rar_options, engine), offsetof(rar_options, channels), offsetof(rar_options, slice_elems),
     offsetof(rar_options, block_threads), offsetof(rar_options, timeout_ns),
     offsetof(rar_options, skip_pointer_check), offsetof(rar_options, fault_mode),
     offsetof(rar_options, fault_rank), offsetof(rar_options, fault_delay_ns),
     offsetof(rar_options, fused_path), offsetof(rar_options, hier_group), offsetof(rar_options, protocol),
-    offsetof(rar_options, slice_block));
+    offsetof(rar_options, slice_block), offsetof(rar_options, trace));
   return 0;
 }'''
     with tempfile.TemporaryDirectory() as d:
@@ -74,7 +74,7 @@ int main(void) {
     assert vals == [ctypes.sizeof(O), O.engine.offset, O.channels.offset, O.slice_elems.offset,
                     O.block_threads.offset, O.timeout_ns.offset, O.skip_pointer_check.offset,
                     O.fault_mode.offset, O.fault_rank.offset, O.fault_delay_ns.offset, O.fused_path.offset,
-                    O.hier_group.offset, O.protocol.offset, O.slice_block.offset]
+                    O.hier_group.offset, O.protocol.offset, O.slice_block.offset, O.trace.offset]
 
 
 def test_host_side_errors_without_gpu(lib):

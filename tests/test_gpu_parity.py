@@ -518,6 +518,56 @@ def test_epoch_wrap_around(rar, dev, engine):
                 assert_bits_equal(rows, ref, f"{engine}: epoch {start + k + 1:#x}")
 
 
+@pytest.mark.parametrize("engine", ["ring", "ring_bidir", "tree"])
+def test_step_trace_finds_the_straggler(rar, dev, engine):
+    """"Ring All-Reduce, in depth", "Failure modes": a straggler is found by
+    comparing per-rank step times.  With a pause injected before every slice
+    of one rank, the step trace shows that rank with by far the most work
+    time (and, on the one-way ring, its right neighbour with the most wait
+    time); the results stay exact."""
+    p, n, slow = 8, 8 * 40000 + 3, 3
+    host = gen(p, n, "float32", ("normal", 1.0), 77)
+    ref, _ = oracle_expect(host, "float32", "sum", engine)
+    _, rows = upload(host, dev)
+    with rar.Handle(0, **handle_opts(engine, trace=True, fault_mode="delay", fault_rank=slow,
+                                     fault_delay_ns=20_000, slice_elems=2048)) as h:
+        h.allreduce(rows)
+        h.check()
+        work, wait = h.trace(p)
+    assert_bits_equal(rows, ref, f"{engine} traced straggler")
+    steps = 2 * (p - 1) if engine != "tree" else 2 * 3
+    assert all(len(w) == steps for w in work + wait)
+    total = [sum(w) for w in work]
+    order = sorted(range(p), key=total.__getitem__)
+    assert order[-1] == slow and total[slow] > 3 * total[order[-2]], total
+    if engine == "ring":
+        waited = [sum(w) for w in wait]
+        assert max(range(p), key=waited.__getitem__) == (slow + 1) % p, waited
+        # every rank works at every step of the ring
+        assert all(x > 0 for w in work for x in w)
+
+
+def test_step_trace_refusals(rar, dev):
+    """rar_trace reports only a traced call of an executor with progress
+    words: not an untraced call, nor the fused engine, nor another p."""
+    host = gen(4, 4 * 3000, "float32", ("normal", 1.0), 78)
+    _, rows = upload(host, dev)
+    with rar.Handle(0, engine="ring", protocol="simple") as h:
+        h.allreduce(rows)
+        with pytest.raises(rar.RarError):
+            h.trace(4)
+    with rar.Handle(0, engine="fused", trace=True) as h:
+        h.allreduce(rows)
+        with pytest.raises(rar.RarError):
+            h.trace(4)
+    with rar.Handle(0, engine="ring", protocol="simple", trace=True) as h:
+        h.allreduce(rows)
+        work, wait = h.trace(4)
+        assert len(work) == 4 and len(work[0]) == 6
+        with pytest.raises(rar.RarError):
+            h.trace(5)
+
+
 def test_ring_straggler_keeps_results(rar, dev):
     """An injected slow rank (pause before every slice) changes timing only."""
     host = gen(4, 4 * 3000 + 1, "float32", ("normal", 1.0), 10)

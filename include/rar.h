@@ -190,7 +190,7 @@ typedef struct {
 #define RAR_LL_MAILBOX_BYTES (64u << 20)
 
 /* Create a handle on `device`; allocates the ring and tree engines' progress
- * words, counters and status word there (about 8.5 MB) and the low-latency mailbox
+ * words, counters and status word there (about 33 MB) and the low-latency mailbox
  * (RAR_LL_MAILBOX_BYTES).  opt may be NULL.
  * Errors: RAR_EINVAL (out NULL, bad device or option), RAR_ENOMEM,
  * RAR_ECUDA. */

@@ -15,9 +15,9 @@ namespace {
 using namespace rar;
 
 constexpr int kMaxRingCtas = 8192;           // counters capacity; CTAs of a ring or tree launch
-// progress words: one per warp of a ring launch, one per (rank, slice) of a
-// tree launch (8 MB)
-constexpr int kFlagWords = 1 << 20;
+// progress words: one per warp of a ring launch, one per (rank, slice, warp)
+// of a tree launch (32 MB)
+constexpr int kFlagWords = 1 << 22;
 static_assert(kFlagWords >= kMaxRingCtas * kRingMaxWarps, "a progress word per ring warp");
 constexpr int kRingPhases = 3;               // counter arrays: one per ring launch of a call
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
@@ -404,7 +404,8 @@ int launch_tree_ll_phase(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
 // it takes part in, 2 (p - 1) in all), with the largest scale that fits the
 // co-resident grid, so that every CTA carries about the same work; when even
 // scale 1 does not fit, or `channels` is set, every rank gets the same
-// number.  Slices: up to 128 KB, with one progress word per (rank, slice).
+// number.  Slices: up to 128 KB, with one progress word per (rank, slice,
+// warp).
 int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int dtype, int op, bool vec16,
                          cudaStream_t stream) {
     const int threads = h->opt.block_threads ? h->opt.block_threads : 512;
@@ -430,8 +431,8 @@ int launch_tree_schedule(rar_ctx *h, const RankPtrs &ptrs, int p, size_t n, int 
                                     kRingMaxSliceBytes / elem_bytes(dtype));
     }
     slice = std::max<long long>(16, (slice + 15) / 16 * 16);
-    // one progress word per (rank, slice)
-    while ((long long)p * (((long long)n + slice - 1) / slice) > kFlagWords) slice *= 2;
+    // one progress word per (rank, slice, warp)
+    while ((long long)p * (((long long)n + slice - 1) / slice) * (threads / 32) > kFlagWords) slice *= 2;
     cudaError_t ce = cudaMemsetAsync(h->recv_counts, 0, sizeof(unsigned long long) * (size_t)p, stream);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "clearing the send counters");
     RingArgs a = handle_ring_args(h, ptrs, p, n, 0, (long long)n);  // the tree's order ignores the index

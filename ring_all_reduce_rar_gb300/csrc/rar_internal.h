@@ -132,7 +132,7 @@ struct RingArgs {
     unsigned *finish_count;
     int flag_capacity;                // progress words to clear when the epoch wraps
     unsigned long long *flags;        // progress words: [p * channels * warps per CTA] for the
-                                      // ring executor, [p * slices] for the tree executor
+                                      // ring executor, [p * slices * warps per CTA] for the tree executor
     // The low-latency mailbox (ll.cu): words tagged with the
     // launch's epoch, so any launch that wraps the epoch clears all of them;
     // slot_words = words per (rank, step) slot.  NULL / 0 where unused.

@@ -26,8 +26,12 @@
 // every CTA carries about the same work: CTA j of rank r takes slices j,
 // j + G_r, ... and runs only the rank's active steps.
 //
-// Hand-offs: one progress word per (rank, slice), holding
-// (epoch << 32) | (active steps the rank has completed on that slice).  A
+// Hand-offs: one progress word per (rank, slice, warp), holding
+// (epoch << 32) | (active steps the rank has completed on that slice).  As
+// in the ring executor, every rank cuts the same slices and thread t always
+// takes the same vectors and elements of a slice, so warp w only ever reads
+// what warp w of the peer wrote, and waits for that warp alone: no CTA
+// barrier sits between slices.  A
 // parent at reduce level l needs its child c's subtree partial, complete
 // once c has done all its reduce levels (w_c - 1 steps); a child at its
 // broadcast level needs its parent's final value, complete once the parent
@@ -131,7 +135,7 @@ __device__ __forceinline__ void tree_slice(const char *src, char *dst, long long
 
 template <int DT, int OP, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __grid_constant__ RingArgs a) {
-    __shared__ int s_stop, s_rank, s_j, s_g;
+    __shared__ int s_rank, s_j, s_g;
     __shared__ unsigned long long s_trace_t0, s_trace_t1;  // (step trace)
     const int p = a.p;
     const int L = tree_levels(p);
@@ -151,7 +155,9 @@ __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __
     const int r = s_rank, j = s_j, G = s_g;
     char *mine = rank_ptr(a.bufs, p, r);
     const long long nsl = (a.n + a.slice - 1) / a.slice;
-    unsigned long long *my_flags = a.flags + (long long)r * nsl;  // one per slice
+    const int W = blockDim.x >> 5;  // warps per CTA: a progress word each, per slice
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned long long *my_flags = a.flags + (long long)r * nsl * W + w;  // [slice * W]
     const bool muted = a.fault_mode == RAR_FAULT_MUTE && r == a.fault_rank;
     const bool slow = a.fault_mode == RAR_FAULT_DELAY && r == a.fault_rank;
     // the rank's active steps: reduce levels 0 .. m - 1, then (not the root)
@@ -186,18 +192,18 @@ __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __
             const int need = up ? tree_weight(peer, p, L) - 1 : tree_weight(peer, p, L);
             const char *src = rank_ptr(a.bufs, p, peer);
             for (long long sl = s_first; sl < g1; sl += G) {
-                if (threadIdx.x == 0) {
-                    if (a.trace) s_trace_t0 = global_ns();
-                    bool ok = need > 0 ? ring_wait(a, epoch, a.flags + (long long)peer * nsl + sl,
-                                                   ((unsigned long long)epoch << 32) | (unsigned)need, r, step, sl,
-                                                   peer)
-                                       : ld_relaxed_u32(a.abort_word) != epoch;
-                    if (a.trace) s_trace_t1 = global_ns();
+                // this warp's part of the slice: the same warp of the peer
+                int ok = 1;
+                if (lane == 0) {
+                    if (a.trace && w == 0) s_trace_t0 = global_ns();
+                    ok = need > 0 ? ring_wait(a, epoch, a.flags + ((long long)peer * nsl + sl) * W + w,
+                                              ((unsigned long long)epoch << 32) | (unsigned)need, r, step, sl, peer)
+                                  : ld_relaxed_u32(a.abort_word) != epoch;
+                    if (a.trace && w == 0) s_trace_t1 = global_ns();
                     if (ok && slow) ring_delay(a.fault_delay_ns);
-                    s_stop = ok ? 0 : 1;
                 }
-                __syncthreads();
-                if (s_stop) goto done;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) goto done;
+                __syncwarp();  // orders lane 0's acquire before the other lanes' reads
                 const long long lo = sl * a.slice;
                 const long long hi = lo + a.slice < a.n ? lo + a.slice : a.n;
                 // from level 1 up the child holds a partial of its subtree;
@@ -205,13 +211,15 @@ __global__ void __launch_bounds__(kTreeThreads, 3) tree_executor_kernel(const __
                 const bool root_last = r == 0 && l == L - 1;
                 tree_slice<DT, OP, VEC>(src, mine, lo, hi, up, up && root_last, up && l > 0, up || l == 0,
                                         up && !root_last, a.inv_p);
-                __syncthreads();
-                if (threadIdx.x == 0) {
-                    atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // the peer sent
-                    // the release store orders the CTA's slice stores
-                    // (ordered before it by the barrier) ahead of the word
-                    st_release_u64(my_flags + sl, ((unsigned long long)epoch << 32) | (unsigned)(t + 1));
-                    if (a.trace) trace_add(a, r, step, s_trace_t0, s_trace_t1);
+                // the warp barrier orders the lanes' stores of this part
+                // before lane 0's release of the warp's word
+                __syncwarp();
+                if (lane == 0) {
+                    st_release_u64(my_flags + sl * W, ((unsigned long long)epoch << 32) | (unsigned)(t + 1));
+                    if (w == 0) {
+                        atomicAdd(&a.recv_counts[peer], (unsigned long long)(hi - lo));  // the peer sent
+                        if (a.trace) trace_add(a, r, step, s_trace_t0, s_trace_t1);
+                    }
                 }
             }
         }

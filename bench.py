@@ -110,7 +110,7 @@ def hbm_peak():
 ENGINE_SOURCES = {
     "fused": ("rar_internal.h", "elem_ops.cuh", "fused_impl.cuh", "fused.cu", "fused_stream.cu", "rar_api.cu"),
     "ring": ("rar_internal.h", "elem_ops.cuh", "flag_sync.cuh", "ring.cu", "rar_api.cu"),
-    "tree": ("rar_internal.h", "elem_ops.cuh", "flag_sync.cuh", "tree.cu", "rar_api.cu"),
+    "tree": ("rar_internal.h", "elem_ops.cuh", "flag_sync.cuh", "tree_plan.h", "tree.cu", "rar_api.cu"),
 }
 ENGINE_SOURCES["ring_bidir"] = ENGINE_SOURCES["ring"]
 

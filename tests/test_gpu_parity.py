@@ -420,6 +420,55 @@ def test_tree_weighted_ctas_any_group_size(rar, dev):
             assert got == [(n if r else 0) + n * len(_tree_children(r, p)) for r in range(p)]
 
 
+def test_stream_order_with_programmatic_launches(rar, dev):
+    """The fused kernels are launched so that they may be scheduled while
+    the previous kernel of the stream drains; each waits for it before it
+    touches a rank buffer.  A chain on one stream, with no synchronisation
+    in between -- fused all-reduce, a torch kernel that rewrites the
+    buffers, fused again, the ring executor, the tree executor, fused --
+    must give the oracle's result for every step of the chain."""
+    p, n = 8, 8 * 50000 + 3
+    host = gen(p, n, "float32", ("uniform", -1.0, 1.0), 81)
+    _, rows = upload(host, dev)
+    big = torch.stack([t for t in host]).clone()  # (p, n) CPU copy of the inputs
+    stream = torch.cuda.current_stream()
+
+    def expect(x, order):
+        bufs = [w.to_storage_numpy(x[r]).copy() for r in range(p)]
+        if order == "tree":
+            oracle.tree_fold(bufs, "float32", "sum")
+        else:
+            oracle.simulate(bufs, "float32", "sum")
+        return torch.from_numpy(np.stack(bufs))
+
+    with rar.Handle(0, engine="fused") as hf, rar.Handle(0, engine="ring", protocol="simple") as hr, \
+            rar.Handle(0, engine="tree", protocol="simple") as ht:
+        hf.allreduce(rows, stream=stream)
+        ref = expect(big, "ring")
+        for r in range(p):  # a kernel of another library between two calls
+            rows[r].mul_(0.5).add_(float(r))
+        ref = ref * 0.5 + torch.arange(p, dtype=torch.float32)[:, None]
+        hf.allreduce(rows, stream=stream)
+        ref = expect(ref, "ring")
+        for r in range(p):
+            rows[r].sub_(float(r))
+        ref = ref - torch.arange(p, dtype=torch.float32)[:, None]
+        hr.allreduce(rows, stream=stream)
+        ref = expect(ref, "ring")
+        for r in range(p):
+            rows[r].mul_(0.25)
+        ref = ref * 0.25
+        ht.allreduce(rows, stream=stream)
+        ref = expect(ref, "tree")
+        hf.allreduce(rows, stream=stream)
+        ref = expect(ref, "ring")
+        for h in (hf, hr, ht):
+            h.check()
+    torch.cuda.synchronize()
+    got = torch.stack([t.cpu() for t in rows])
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+
+
 def test_ring_back_to_back_calls_reuse_flags(rar, dev):
     host = gen(4, 4099, "float32", ("uniform", -1.0, 1.0), 3)
     ref, _ = oracle_expect(host, "float32", "sum", "ring")

@@ -615,6 +615,40 @@ def run_configs(args):
         torch.cuda.empty_cache()
 
 
+def run_trace(args):
+    """The executors' step trace (rar_options.trace) on one workload: per
+    engine, the share of time the first warp of each CTA spent waiting for its
+    neighbour, and per schedule step the mean over ranks of the wait and work
+    time summed over the rank's CTAs; one JSON line per engine.  A traced call
+    runs the traced kernel instantiation, so its times are not bench times."""
+    import ring_all_reduce_rar_gb300 as rar
+    rar.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cfg = w.WORKLOADS[args.workload]
+    p, dtype, op = cfg["p"], cfg["dtype"], args.op or cfg["ops"][0]
+    n = args.n or cfg["n"]
+    big, rows = w.make_inputs(p, n, dtype, cfg["dist"], w.seed_of(cfg["index"]), device=dev)
+    for eng in ("ring", "ring_bidir", "tree"):
+        opts = dict(engine=eng, trace=True, **({} if eng == "ring_bidir" else dict(protocol="simple")))
+        with rar.Handle(0, skip_pointer_check=True, **opts) as h:
+            for _ in range(args.warmup):
+                h.allreduce(rows, op=op)
+            torch.cuda.synchronize()
+            h.check()
+            work, wait = h.trace(p)
+        steps = len(work[0])
+        tw, tt = sum(map(sum, work)), sum(map(sum, wait))
+        print(json.dumps({
+            "workload": args.workload, "n": n, "op": op, "engine": eng, "steps": steps,
+            "wait_share": round(tt / max(1, tw + tt), 4),
+            "wait_us_per_step": [round(sum(wait[r][s] for r in range(p)) / p / 1e3, 1) for s in range(steps)],
+            "work_us_per_step": [round(sum(work[r][s] for r in range(p)) / p / 1e3, 1) for s in range(steps)],
+        }), flush=True)
+    del big, rows
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -670,6 +704,8 @@ def main():
                     help="per-call time of the smallest buffers for p = 2 ... 64 (fixed cost + step latency)")
     ap.add_argument("--configs", action="store_true",
                     help="device time per call of every workload on every engine (not the benchmark line)")
+    ap.add_argument("--trace", action="store_true",
+                    help="step trace of the ring, bidirectional ring and tree executors on --workload")
     ap.add_argument("--workload", choices=sorted(w.WORKLOADS), default="p8_n1073741824_bf16")
     ap.add_argument("--op", choices=["sum", "avg", "max"], default=None)
     ap.add_argument("--n", type=int, default=None,
@@ -686,6 +722,8 @@ def main():
         run_next(args)
     elif args.configs:
         run_configs(args)
+    elif args.trace:
+        run_trace(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

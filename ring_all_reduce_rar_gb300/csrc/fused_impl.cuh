@@ -498,12 +498,18 @@ static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int
         return launch_persistent(fused_tree_order_kernel<DT, OP, P, false>, a, a.n, threads, stream);
     }
     if (vec16) {
-        // a buffer that one vector per thread covers within one wave of
-        // CTAs: one vector per thread, all in flight at once, instead of U
-        // per thread one after the other (at most a few tiles, each of which
-        // may cross chunk boundaries)
+        // One vector per thread for a buffer that the one-vector kernel
+        // covers in at most two waves of its co-resident grid.  The U-vector
+        // kernel's registers cannot hold all of its p * U loads at once, so it
+        // has about as many bytes in flight per thread as the one-vector
+        // kernel, on half the threads: below a full grid the one-vector
+        // kernel keeps twice the loads in flight (GB300, p = 8: 1-2 M
+        // elements per rank 27-40% faster, 2.4 M fp32 10%).  From about two
+        // waves on the two kernels are within a few percent either way, and
+        // the U-vector kernel is ahead at 25 MB per rank (p = 8 fp32, 2%).
         const long long nvec = (a.n + VE - 1) / VE;
-        if (U > 1 && nvec <= (long long)sm_count_cached() * threads)
+        if (U > 1 && nvec <= 2ll * sm_count_cached() *
+                                 blocks_per_sm_of(fused_ring_order_kernel<DT, OP, P, 1, true>, threads) * threads)
             return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, true>, a, nvec, threads, stream);
         return launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, a, (nvec + U - 1) / U, threads,
                                  stream);

@@ -129,6 +129,88 @@ __device__ __forceinline__ void fused_fold_element(const FusedArgs &a, int p, in
     for (int r = 0; r < p; r++) store_elem<DT>(rank_ptr(a.bufs, p, r), i, acc);
 }
 
+// A 16-byte vector v whose elements lie in more than one chunk, the first of
+// them in chunk ca, folded from global memory by a whole warp.  The warp
+// passes over the ranks from ca on, lane j loading the whole vector of rank
+// (ca + j0 + j) mod p as pass step j0 + j, 32 ranks at a time; lane l < VE
+// folds element l, of chunk ca + d_l, taking pass step j as its hop j - d_l
+// (the lag of the streaming path's segments), so every element is folded in
+// its own chunk's order, as fused_fold_element folds it.  All 32 lanes of a
+// converged warp call it with the same v and ca; every lane gets the vector.
+template <int DT, int OP>
+__device__ __forceinline__ uint4 warp_fold_straddling_vector(const FusedArgs &a, int p, long long base,
+                                                             long long extra, long long v, int ca) {
+    constexpr int EB = ElemInfo<DT>::bytes;
+    constexpr int VE = 16 / EB;
+    constexpr int hop = HopOf<OP>::value;
+    const int lane = threadIdx.x & 31;
+    const int my_l = lane < VE ? lane : VE - 1;  // (lanes >= VE shadow the last element)
+    // d_l: the chunks after ca that start at or before element l
+    const long long gi = a.first + v * VE + my_l;
+    int d = 0;
+    while (ca + d + 1 < p && chunk_start(ca + d + 1, base, extra) <= gi) d++;
+    const int steps = p + __shfl_sync(0xffffffffu, d, 31);  // (lane 31 holds the last element's d)
+    const int wi = (my_l * EB) >> 2;                          // the word holding this lane's element
+    uint32_t acc = 0;
+    for (int j0 = 0; j0 < steps; j0 += 32) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (j0 + lane < steps)
+            x = __ldcg(reinterpret_cast<const uint4 *>(rank_ptr(a.bufs, p, (ca + j0 + lane) % p)) + v);
+        const int jn = steps - j0 < 32 ? steps - j0 : 32;
+        for (int j = 0; j < jn; j++) {
+            const uint32_t w0 = __shfl_sync(0xffffffffu, x.x, j), w1 = __shfl_sync(0xffffffffu, x.y, j);
+            const uint32_t w2 = __shfl_sync(0xffffffffu, x.z, j), w3 = __shfl_sync(0xffffffffu, x.w, j);
+            const uint32_t w = wi == 0 ? w0 : wi == 1 ? w1 : wi == 2 ? w2 : w3;
+            const int k = j0 + j - d;
+            if (lane < VE && k >= 0 && k < p) {
+                // the element in the low half of a word, as load_elem gives it
+                const uint32_t e = contrib_word<DT, OP>(EB == 4 ? w : (w >> (16 * (my_l & 1))) & 0xFFFFu, a.inv_p);
+                acc = k == 0 ? e : hop_word<DT, hop>(acc, e);
+            }
+        }
+    }
+    if constexpr (OP == OP_AVG) acc = scale_word<DT>(acc, a.inv_p);
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        if constexpr (EB == 4) out[q] = __shfl_sync(0xffffffffu, acc, q);
+        else
+            out[q] = (__shfl_sync(0xffffffffu, acc, 2 * q) & 0xFFFFu) |
+                     ((__shfl_sync(0xffffffffu, acc, 2 * q + 1) & 0xFFFFu) << 16);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// The vectors across a chunk boundary of a whole all-reduce on the
+// per-thread path (16-byte aligned ranks), which the main kernel left out
+// (straddle_pass): warp w takes the start of chunk w + 1 and, where that
+// start is not vector-aligned, folds the vector holding it and stores it to
+// every rank; a vector holding several starts goes with the first.  Its own
+// launch, so that this rarely used code does not weigh on the main kernel's
+// registers; it runs after the main kernel (pdl_wait), like any next kernel.
+template <int DT, int OP>
+__global__ void __launch_bounds__(kFusedThreads) fused_straddle_kernel(const __grid_constant__ FusedArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr int VE = 16 / ElemInfo<DT>::bytes;
+    const int p = a.p;
+    const long long base = a.n_total / p, extra = a.n_total % p;
+    const int c = 1 + (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (c >= p) return;  // (the tests below are warp-uniform)
+    const long long b = chunk_start(c, base, extra) - a.first;  // chunk c's first element, local index
+    if (b <= 0 || b % VE == 0) return;                           // outside the range, or vector-aligned
+    const long long sv = b / VE;
+    if (sv >= a.n / VE) return;  // the ragged tail: the main kernel folds it element by element
+    // Chunk c - 1 starts at bp.  If bp lies inside the same vector (not at
+    // its first element), the vector goes with chunk c - 1's start; else
+    // bp <= the vector's first element < b, so that element is in chunk
+    // c - 1.
+    const long long bp = chunk_start(c - 1, base, extra) - a.first;
+    if (bp > sv * VE && bp / VE == sv) return;
+    const uint4 x = warp_fold_straddling_vector<DT, OP>(a, p, base, extra, sv, c - 1);
+    for (int r = threadIdx.x & 31; r < p; r += 32) __stcs(reinterpret_cast<uint4 *>(rank_ptr(a.bufs, p, r)) + sv, x);
+}
+
 template <int DT, int OP, int P, int U, bool VEC>
 __global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const __grid_constant__ FusedArgs a) {
     pdl_wait();
@@ -162,6 +244,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const _
                     fused_fold_vectors<DT, OP, P, 1>(a, p, ca, v, 0);
                     continue;
                 }
+                if (a.straddle_pass) continue;  // (fused_straddle_kernel folds it)
             }
             for (int l = 0; l < VE; l++) {
                 const long long i = e0 + l;
@@ -487,6 +570,17 @@ static cudaError_t launch_persistent(K kernel, const FusedArgs &a, long long wor
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Whether a chunk start inside the launch's index range is not 16-byte
+// aligned (so that a vector lies across the boundary).
+static bool has_unaligned_chunk_start(const FusedArgs &a, int ve) {
+    const long long base = a.n_total / a.p, extra = a.n_total % a.p;
+    for (int c = 1; c < a.p; c++) {
+        const long long b = chunk_start(c, base, extra) - a.first;
+        if (b > 0 && b < a.n && b % ve != 0) return true;
+    }
+    return false;
+}
+
 template <int DT, int OP, int P>
 static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int threads, cudaStream_t stream) {
     constexpr int VE = 16 / ElemInfo<DT>::bytes;
@@ -511,8 +605,18 @@ static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int
         if (U > 1 && nvec <= 2ll * sm_count_cached() *
                                  blocks_per_sm_of(fused_ring_order_kernel<DT, OP, P, 1, true>, threads) * threads)
             return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, true>, a, nvec, threads, stream);
-        return launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, a, (nvec + U - 1) / U, threads,
-                                 stream);
+        // Beyond p = 8 a vector across a chunk boundary costs its thread p
+        // dependent element folds per element (p = 64 x 250,000 bf16: 108 us
+        // against 37 us with aligned chunk starts), so those vectors go to a
+        // warp each in a pass of their own.
+        FusedArgs b = a;
+        b.straddle_pass = a.phase == PHASE_ALL && a.p > 8 && has_unaligned_chunk_start(a, VE) ? 1 : 0;
+        cudaError_t e = launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, b, (nvec + U - 1) / U,
+                                          threads, stream);
+        if (e != cudaSuccess || !b.straddle_pass) return e;
+        const unsigned blocks = (unsigned)(((long long)(a.p - 1) * 32 + kFusedThreads - 1) / kFusedThreads);
+        e = launch_pdl(fused_straddle_kernel<DT, OP>, dim3(blocks), dim3(kFusedThreads), 0, stream, b);
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, false>, a, a.n, threads, stream);
 }

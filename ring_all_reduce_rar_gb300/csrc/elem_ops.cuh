@@ -215,7 +215,7 @@ __device__ __forceinline__ int chunk_of(long long i, long long base, long long e
     long long big = extra * (base + 1);
     return (int)(i < big ? i / (base + 1) : extra + (i - big) / base);
 }
-__host__ __device__ __forceinline__ long long chunk_start(int c, long long base, long long extra) {
+__device__ __forceinline__ long long chunk_start(int c, long long base, long long extra) {
     return (long long)c * base + (c < extra ? c : extra);
 }
 

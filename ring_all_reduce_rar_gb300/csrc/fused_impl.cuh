@@ -183,7 +183,7 @@ __device__ __forceinline__ uint4 warp_fold_straddling_vector(const FusedArgs &a,
 
 // The vectors across a chunk boundary of a whole all-reduce on the
 // per-thread path (16-byte aligned ranks), which the main kernel left out
-// (straddle_pass): warp w takes the start of chunk w + 1 and, where that
+// (its straddle_pass): warp w takes the start of chunk w + 1 and, where that
 // start is not vector-aligned, folds the vector holding it and stores it to
 // every rank; a vector holding several starts goes with the first.  Its own
 // launch, so that this rarely used code does not weigh on the main kernel's
@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(kFusedThreads) fused_straddle_kernel(const __g
 }
 
 template <int DT, int OP, int P, int U, bool VEC>
-__global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const __grid_constant__ FusedArgs a) {
+__global__ void __launch_bounds__(kFusedThreads)
+    fused_ring_order_kernel(const __grid_constant__ FusedArgs a, int straddle_pass) {
     pdl_wait();
     pdl_launch_dependents();
     const int p = P > 0 ? P : a.p;
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_ring_order_kernel(const _
                     fused_fold_vectors<DT, OP, P, 1>(a, p, ca, v, 0);
                     continue;
                 }
-                if (a.straddle_pass) continue;  // (fused_straddle_kernel folds it)
+                if (straddle_pass) continue;  // (fused_straddle_kernel folds it)
             }
             for (int l = 0; l < VE; l++) {
                 const long long i = e0 + l;
@@ -558,15 +559,15 @@ static int sm_count_cached() {
     return v > 0 ? v : 1;
 }
 
-template <typename K>
+template <typename K, typename... Extra>
 static cudaError_t launch_persistent(K kernel, const FusedArgs &a, long long work_items, int threads,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, Extra... extra) {
     const int sms = sm_count_cached();
     const long long want = (work_items + threads - 1) / threads;
     long long grid = (long long)sms * blocks_per_sm_of(kernel, threads);
     if (grid > want) grid = want;
     if (grid < 1) grid = 1;
-    cudaError_t e = launch_pdl(kernel, dim3((unsigned)grid), dim3((unsigned)threads), 0, stream, a);
+    cudaError_t e = launch_pdl(kernel, dim3((unsigned)grid), dim3((unsigned)threads), 0, stream, a, extra...);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -575,7 +576,7 @@ static cudaError_t launch_persistent(K kernel, const FusedArgs &a, long long wor
 static bool has_unaligned_chunk_start(const FusedArgs &a, int ve) {
     const long long base = a.n_total / a.p, extra = a.n_total % a.p;
     for (int c = 1; c < a.p; c++) {
-        const long long b = chunk_start(c, base, extra) - a.first;
+        const long long b = (long long)c * base + (c < extra ? c : extra) - a.first;  // chunk_start(c)
         if (b > 0 && b < a.n && b % ve != 0) return true;
     }
     return false;
@@ -604,21 +605,20 @@ static cudaError_t launch_fused_p(const FusedArgs &a, bool tree, bool vec16, int
         const long long nvec = (a.n + VE - 1) / VE;
         if (U > 1 && nvec <= 2ll * sm_count_cached() *
                                  blocks_per_sm_of(fused_ring_order_kernel<DT, OP, P, 1, true>, threads) * threads)
-            return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, true>, a, nvec, threads, stream);
+            return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, true>, a, nvec, threads, stream, 0);
         // Beyond p = 8 a vector across a chunk boundary costs its thread p
         // dependent element folds per element (p = 64 x 250,000 bf16: 108 us
         // against 37 us with aligned chunk starts), so those vectors go to a
         // warp each in a pass of their own.
-        FusedArgs b = a;
-        b.straddle_pass = a.phase == PHASE_ALL && a.p > 8 && has_unaligned_chunk_start(a, VE) ? 1 : 0;
-        cudaError_t e = launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, b, (nvec + U - 1) / U,
-                                          threads, stream);
-        if (e != cudaSuccess || !b.straddle_pass) return e;
+        const int straddle_pass = a.phase == PHASE_ALL && a.p > 8 && has_unaligned_chunk_start(a, VE) ? 1 : 0;
+        cudaError_t e = launch_persistent(fused_ring_order_kernel<DT, OP, P, U, true>, a, (nvec + U - 1) / U,
+                                          threads, stream, straddle_pass);
+        if (e != cudaSuccess || !straddle_pass) return e;
         const unsigned blocks = (unsigned)(((long long)(a.p - 1) * 32 + kFusedThreads - 1) / kFusedThreads);
-        e = launch_pdl(fused_straddle_kernel<DT, OP>, dim3(blocks), dim3(kFusedThreads), 0, stream, b);
+        e = launch_pdl(fused_straddle_kernel<DT, OP>, dim3(blocks), dim3(kFusedThreads), 0, stream, a);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
-    return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, false>, a, a.n, threads, stream);
+    return launch_persistent(fused_ring_order_kernel<DT, OP, P, 1, false>, a, a.n, threads, stream, 0);
 }
 
 template <int DT, int OP>

@@ -505,7 +505,6 @@ int run(rar_ctx *h, void *const *bufs, int p, size_t n, int dtype, int op, int p
         a.timeout_ns = h->opt.timeout_ns ? h->opt.timeout_ns : kDefaultTimeoutNs;
         a.fault_mode = h->opt.fault_mode;
         a.fault_rank = h->opt.fault_rank;
-        a.straddle_pass = 0;  // (launch_fused sets it where it launches that pass)
         const bool tree = engine == RAR_ENGINE_FUSED_TREE && phase != PHASE_AG;
         if (hier) {
             if (engine != RAR_ENGINE_FUSED || phase != PHASE_ALL || h->opt.fused_path == 2)

@@ -93,9 +93,6 @@ struct FusedArgs {
     unsigned long long timeout_ns;
     int fault_mode;
     int fault_rank;
-    // per-thread path, whole all-reduce: the vectors across a chunk boundary
-    // are left to fused_straddle_kernel, launched right after
-    int straddle_pass;
 };
 
 // Which rings a ring launch runs (the hierarchical schedule uses 1 and 2).

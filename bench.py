@@ -615,6 +615,38 @@ def run_configs(args):
         torch.cuda.empty_cache()
 
 
+MID_SHAPES = [(8, 500_000, "bfloat16"), (8, 1_000_000, "bfloat16"), (8, 2_000_000, "bfloat16"),
+              (8, 1_000_000, "float32"), (8, 2_400_000, "float32"), (4, 1_000_000, "float32"),
+              (4, 2_000_000, "float32"), (16, 500_000, "bfloat16"), (16, 524_288, "bfloat16"),
+              (24, 500_000, "bfloat16"), (32, 500_000, "bfloat16"), (32, 524_288, "bfloat16"),
+              (32, 500_000, "float32"), (40, 1_048_576, "bfloat16"), (64, 250_000, "bfloat16"),
+              (64, 262_144, "bfloat16")]
+
+
+def run_mid(args):
+    """The fused engine on mid-size buffers (1-16 MB per rank, p = 4 ... 64,
+    chunk starts aligned to 16 bytes or not): device time per call and the
+    fraction of the 2 p N e roofline, one JSON line per shape.  Values N(0,
+    1e-2) (fp32 N(0, 1e-3)), sum."""
+    import ring_all_reduce_rar_gb300 as rar
+    rar.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak = hbm_peak()[0]
+    for p, n, dtype in MID_SHAPES:
+        e = torch.tensor([], dtype=w.TORCH_DTYPES[dtype]).element_size()
+        dist = ("normal", 1e-3 if dtype == "float32" else 1e-2)
+        big, rows = w.make_inputs(p, n, dtype, dist, 5, device=dev)
+        us = device_us_per_call(rar, VARIANTS["fused"], rows, "sum", 50)
+        chunk = n // p
+        print(json.dumps({"p": p, "n": n, "dtype": dtype, "chunk_starts_aligned": all(
+            ((c * chunk + min(c, n % p)) * e) % 16 == 0 for c in range(1, p)),
+            "us_per_call": round(us, 2), "algbw_gbs": round(p * n * e / us / 1e3, 2),
+            "roofline_frac": round(2 * p * n * e / us / 1e3 / peak, 4)}), flush=True)
+        del big, rows
+        torch.cuda.empty_cache()
+
+
 def run_trace(args):
     """The executors' step trace (rar_options.trace) on one workload: per
     engine, the share of time the first warp of each CTA spent waiting for its
@@ -704,6 +736,8 @@ def main():
                     help="per-call time of the smallest buffers for p = 2 ... 64 (fixed cost + step latency)")
     ap.add_argument("--configs", action="store_true",
                     help="device time per call of every workload on every engine (not the benchmark line)")
+    ap.add_argument("--mid", action="store_true",
+                    help="the fused engine on mid-size buffers, p = 4 ... 64 (not the benchmark line)")
     ap.add_argument("--trace", action="store_true",
                     help="step trace of the ring, bidirectional ring and tree executors on --workload")
     ap.add_argument("--workload", choices=sorted(w.WORKLOADS), default="p8_n1073741824_bf16")
@@ -724,6 +758,8 @@ def main():
         run_configs(args)
     elif args.trace:
         run_trace(args)
+    elif args.mid:
+        run_mid(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -25,7 +25,9 @@
  * between GPUs.  Engines (rar_options.engine):
  *   RAR_ENGINE_FUSED       one kernel reads every rank's element once, folds
  *                          in hop order and stores the result to every rank
- *                          (2 p n element moves);
+ *                          (2 p n element moves); on the per-thread path with
+ *                          p > 8, a second small launch folds the vectors that
+ *                          lie across an unaligned chunk start;
  *   RAR_ENGINE_RING        persistent executor: CTA groups play the ranks and
  *                          run the schedule step by step, slice-pipelined,
  *                          handing slices to the right neighbour through

@@ -292,6 +292,21 @@ def test_dtype_op_matrix(rar, dev, engine, dtype, op):
         run_case(rar, dev, host, dtype, op, engine)
 
 
+@pytest.mark.parametrize("dtype,op", [("bfloat16", "sum"), ("bfloat16", "max"), ("float16", "avg"),
+                                      ("float16", "avg_prediv"), ("int32", "sum"), ("float32", "avg")])
+def test_vectors_across_chunk_starts_beyond_p8(rar, dev, dtype, op):
+    """Fused per-thread path, p > 8: the vectors that hold an unaligned
+    chunk start are folded by a warp each in a launch of their own, every
+    element in its own chunk's hop order.  Chunks longer than a vector, and
+    shorter ones, so that one vector holds several chunk starts (and empty
+    chunks when N < p)."""
+    dist = ("uniform_int", -(1 << 20), 21) if dtype == "int32" else ("normal", 1.0)
+    for p in [12, 24, 40]:
+        for n in [37 * p + 5, 3 * p + 1, p + 3, p - 5]:
+            host = gen(p, n, dtype, dist, 31 * p + n)
+            run_case(rar, dev, host, dtype, op, "fused_regs")
+
+
 @pytest.mark.parametrize("engine", SMALL_ENGINES)
 def test_misaligned_pointers_take_element_path(rar, dev, engine):
     """Rank pointers offset by one element (not 16-byte aligned): same bits."""

@@ -64,7 +64,11 @@ __device__ __forceinline__ void fused_fold_vectors(const FusedArgs &a, int p, in
 #pragma unroll
             for (int u = 0; u < U; u++) acc[u] = hop_vec<DT, hop>(acc[u], contrib_vec<DT, OP>(own[k - 1][u], a.inv_p));
     } else {
-        constexpr int G = 8;
+        // loads in batches of G ranks: 4 keeps the kernel at 64-76 registers
+        // (4 CTAs per SM; with 8, 128 registers and 2), which measured
+        // faster wherever the grid takes more than one wave (p = 40 x 1 M
+        // bf16: 62.8 -> 41.1 us) and within 2% elsewhere
+        constexpr int G = 4;
         for (int k0 = 1; k0 < p; k0 += G) {
             uint4 own[G][U];
 #pragma unroll

@@ -11,9 +11,11 @@
 // Work is split into tiles of blockDim.x * U 16-byte vectors, walked by a
 // grid-stride loop over a grid sized to the co-resident CTA count.  A tile
 // inside a single chunk takes the uniform path (one fold order for the whole
-// CTA, all p loads issued before the fold); tiles that cross a chunk
-// boundary or the ragged tail fall back to per-vector and per-element folds,
-// so that no vector lane ever mixes two chunks' orders.
+// CTA; for p = 4, 8, 16 all p loads issued before the fold, for other p in
+// batches of 4 ranks); tiles that cross a chunk boundary or the ragged tail
+// fall back to per-vector and per-element folds, so that no vector lane ever
+// mixes two chunks' orders.  For p > 8 the vectors that hold an unaligned
+// chunk start go to a warp each in a second launch (fused_straddle_kernel).
 #pragma once
 
 #include "elem_ops.cuh"
